@@ -1,0 +1,204 @@
+"""fp64 CPU oracle for exact attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports, links or calls it, and the oracle shares no
+code with that path: inputs reach both sides from the seeded generators only.
+
+The arithmetic lives in ``fa_oracle.c`` (plain C, fp64, OpenMP over rows);
+this module compiles it with gcc on first use and marshals numpy arrays.
+
+Functions and the passages they follow:
+
+* ``attention_fwd`` -- O = softmax(scale Q K^T [+causal mask]) V and the
+  row log-sum-exp L ("6.2 FlashAttention V2 chi tiet", section 6.1 pseudocode;
+  blog.csdn.net FlashAttention-2 page, 3.1.1 forward formula analysis).
+* ``attention_fwd_rows`` -- the same, for selected (b, h, r) rows.
+* ``attention_bwd`` / ``attention_bwd_group`` -- analytic gradients with
+  D = rowsum(dO o O) (blog.csdn.net page, 3.1.2 backward formula analysis;
+  Vietnamese page section 7.3), dK/dV summed over grouped query heads (the
+  blog's MQA/GQA paragraph).
+* ``hadamard`` / ``e4m3_round`` -- random-sign Hadamard rotation and the OCP
+  e4m3 grid used by the FP8 path (FlashAttention-3 summary page, FP8 and
+  incoherent processing section).
+
+Every function is pinned by the CPU tests in ``tests/test_oracle.py`` against
+closed forms, finite differences, library routines and the page's two-block
+worked recurrence.  The FP8 *error level* is parity unpinned by the pages (they
+give only a ratio); see ``fp8_reference``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile fa_oracle.c into oracle/_build/liboracle.so (gcc, -O2, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            L = ctypes.c_long
+            lib.oracle_fwd.argtypes = [P, P, P, P, P, L, L, L, L, L, ctypes.c_int, ctypes.c_double]
+            lib.oracle_fwd_rows.argtypes = [P, P, P, P, L, P, P, L, L, L, L, L, ctypes.c_int, ctypes.c_double]
+            lib.oracle_bwd_group.argtypes = [P, P, P, P, L, L, P, P, P, L, L, L, L, L, ctypes.c_int, ctypes.c_double]
+            lib.oracle_bwd.argtypes = [P, P, P, P, P, P, P, L, L, L, L, L, ctypes.c_int, ctypes.c_double]
+            lib.oracle_hadamard.argtypes = [P, P, P, L, L]
+            lib.oracle_e4m3_round.argtypes = [P, P, L]
+            for name in ("oracle_fwd", "oracle_fwd_rows", "oracle_bwd_group",
+                         "oracle_bwd", "oracle_hadamard", "oracle_e4m3_round"):
+                getattr(lib, name).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x) -> np.ndarray:
+    """Widen to a C-contiguous float64 array (torch tensors are accepted)."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").float().double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        raise ValueError(f"{name}: invalid arguments (code {rc})")
+
+
+def _shapes(q, k):
+    B, Hq, N, d = q.shape
+    Bk, Hkv, Nk, dk = k.shape
+    if (Bk, Nk, dk) != (B, N, d) or Hq % Hkv:
+        raise ValueError("q/k shapes disagree")
+    return B, Hq, Hkv, N, d
+
+
+def attention_fwd(q, k, v, causal: bool, scale: float):
+    """Return (O, L) in fp64; q [B,Hq,N,d], k/v [B,Hkv,N,d]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, N, d = _shapes(q, k)
+    o = np.empty_like(q)
+    lse = np.empty((B, Hq, N), dtype=np.float64)
+    _check(_load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                              B, Hq, Hkv, N, d, int(causal), float(scale)), "oracle_fwd")
+    return o, lse
+
+
+def attention_fwd_rows(q, k, v, rows, causal: bool, scale: float):
+    """O and L for the listed (b, h, r) rows only; returns ([n,d], [n])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Hq, Hkv, N, d = _shapes(q, k)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = rows.shape[0]
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    _check(_load().oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(rows), n,
+                                   _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
+                                   int(causal), float(scale)), "oracle_fwd_rows")
+    return o, lse
+
+
+def attention_bwd(q, k, v, dO, causal: bool, scale: float):
+    """Return (dQ, dK, dV) in fp64 for loss = sum(dO o O)."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, Hq, Hkv, N, d = _shapes(q, k)
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    _check(_load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d,
+                              int(causal), float(scale)), "oracle_bwd")
+    return dq, dk, dv
+
+
+def attention_bwd_group(q, k, v, dO, b: int, g: int, causal: bool, scale: float):
+    """Gradients of one (batch b, key/value head g) group.
+
+    Returns dq [G,N,d] for query heads g*G..g*G+G-1 and dk, dv [N,d].
+    """
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, Hq, Hkv, N, d = _shapes(q, k)
+    G = Hq // Hkv
+    dq = np.empty((G, N, d), dtype=np.float64)
+    dk = np.empty((N, d), dtype=np.float64)
+    dv = np.empty((N, d), dtype=np.float64)
+    _check(_load().oracle_bwd_group(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), int(b),
+                                    int(g), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
+                                    Hkv, N, d, int(causal), float(scale)),
+           "oracle_bwd_group")
+    return dq, dk, dv
+
+
+def hadamard(x, signs=None):
+    """(x o s) H_d / sqrt(d) along the last axis (dense Sylvester product)."""
+    x = _f64(x)
+    d = x.shape[-1]
+    rows = x.size // d
+    out = np.empty_like(x)
+    s = None if signs is None else _f64(signs).reshape(d)
+    _check(_load().oracle_hadamard(_ptr(x), None if s is None else _ptr(s),
+                                   _ptr(out), rows, d), "oracle_hadamard")
+    return out
+
+
+def e4m3_round(x):
+    """Round to the e4m3fn grid (ties to even), saturating at +-448."""
+    x = _f64(x)
+    out = np.empty_like(x)
+    _check(_load().oracle_e4m3_round(_ptr(x), _ptr(out), x.size), "oracle_e4m3_round")
+    return out
+
+
+def fp8_reference(q, k, v, signs, causal: bool, scale: float):
+    """Diagnostic model of the FP8 path's input quantisation.
+
+    Q and K are rotated by the random-sign Hadamard (if ``signs`` is not
+    None), then Q, K and V are each quantised per tensor to e4m3 with
+    sigma = amax / 448, dequantised, and fed to the exact fp64 attention.
+    The rotation is orthogonal, so without quantisation this returns exactly
+    ``attention_fwd(q, k, v)``.  It separates the error of input
+    quantisation from that of a kernel; the error level itself is parity
+    unpinned by the pages, which report only a 2.6x ratio.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if signs is not None:
+        q = hadamard(q, signs)
+        k = hadamard(k, signs)
+
+    def qdq(x):
+        sigma = np.abs(x).max() / 448.0
+        if sigma == 0.0:
+            return x
+        return e4m3_round(x / sigma) * sigma
+
+    return attention_fwd(qdq(q), qdq(k), qdq(v), causal, scale)
