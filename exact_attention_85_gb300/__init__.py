@@ -1,0 +1,74 @@
+"""Exact attention (FlashAttention-2 formulation) for GB300 / sm_103a.
+
+The computation lives in ``libfa.so`` (hand-written CUDA: TMA, tcgen05 MMA
+with tensor-memory accumulators, warp-specialised softmax), reached through
+its C ABI (``include/fa.h``).  This package is the thin Python side: the
+ctypes binding (``_lib``), convenience wrappers that allocate outputs with
+PyTorch, the seeded input generators (``inputs``) and the build script.
+
+PyTorch is used for device memory and streams only.  There is no CPU or
+eager fallback: if the library is missing the calls raise.
+"""
+from __future__ import annotations
+
+import math
+
+from . import _lib
+
+__all__ = ["attention_fwd", "attention_bwd", "hadamard_quant_fp8", "attention_fwd_fp8"]
+
+
+def _default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)
+
+
+def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Returns (O, LSE).  q [B,Hq,N,d], k/v [B,Hkv,N,d]: contiguous CUDA
+    bf16/fp16 tensors; LSE is fp32 [B,Hq,N] (natural log)."""
+    import torch
+    B, Hq, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    _lib.fa_fwd(q, k, v, o, lse, causal, _default_scale(d) if scale is None else scale, stream)
+    return o, lse
+
+
+def attention_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None,
+                  workspace=None, stream=None):
+    """Returns (dQ, dK, dV) from the forward's O and LSE and the incoming dO."""
+    import torch
+    B, Hq, N, d = q.shape
+    if workspace is None:
+        nbytes = _lib.fa_bwd_workspace_bytes(B, Hq, N, d)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    _lib.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal, _default_scale(d) if scale is None else scale,
+                workspace, stream)
+    return dq, dk, dv
+
+
+def hadamard_quant_fp8(x, signs=None, stream=None):
+    """Random-sign Hadamard rotation (if ``signs`` is given) and per-tensor
+    e4m3 quantisation of a bf16 tensor [..., d].  Returns (x8, descale)."""
+    import torch
+    d = x.shape[-1]
+    x8 = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=x.device)
+    descale = torch.empty(1, dtype=torch.float32, device=x.device)
+    ws = torch.empty(_lib.fa_hadamard_quant_workspace_bytes(x.numel() // d, d), dtype=torch.uint8,
+                     device=x.device)
+    _lib.fa_hadamard_quant_fp8(x, signs, x8, descale, ws, stream)
+    return x8, descale
+
+
+def attention_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, causal: bool = False,
+                      scale: float | None = None, stream=None):
+    """FP8 forward: bf16 O and fp32 LSE from e4m3 Q, K, V and their descales."""
+    import torch
+    B, Hq, N, d = q8.shape
+    o = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q8.device)
+    _lib.fa_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, o, lse, causal,
+                    _default_scale(d) if scale is None else scale, stream)
+    return o, lse

@@ -1,0 +1,143 @@
+"""ctypes binding of libfa.so: the C ABI of include/fa.h, same names.
+
+Argument marshalling only -- every step of the computation runs in the CUDA
+kernels.  There is no fallback: if the library has not been built, or a call
+returns an error status, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libfa.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(6)
+FA_FP16, FA_BF16 = 0, 1
+
+EXPORTS = (
+    "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_hadamard_quant_fp8",
+    "fa_hadamard_quant_workspace_bytes", "fa_fwd_fp8", "fa_get_device_status",
+    "fa_selftest_bounded_wait", "fa_status_string",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} ({status})")
+        self.status = status
+
+
+def load():
+    """Load libfa.so (it must already be built: ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                               "(run __graft_entry__.build()); there is no fallback path")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, F, Z, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_long
+        lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
+        lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, Z, P]
+        lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
+        lib.fa_bwd_workspace_bytes.restype = Z
+        lib.fa_hadamard_quant_fp8.argtypes = [P, P, P, P, L, I, P, Z, P]
+        lib.fa_hadamard_quant_workspace_bytes.argtypes = [L, I]
+        lib.fa_hadamard_quant_workspace_bytes.restype = Z
+        lib.fa_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.fa_get_device_status.argtypes = [P]
+        lib.fa_selftest_bounded_wait.argtypes = [I, P]
+        lib.fa_status_string.argtypes = [I]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        for name in ("fa_fwd", "fa_bwd", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
+                     "fa_get_device_status", "fa_selftest_bounded_wait"):
+            getattr(lib, name).restype = I
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int):
+    if status != FA_OK:
+        msg = load().fa_status_string(status).decode()
+        raise FAError(fn, status, msg)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    if t.dtype == torch.float16:
+        return FA_FP16
+    raise TypeError(f"unsupported element type {t.dtype}")
+
+
+def _dims(q, k):
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    return B, Hq, Hkv, N, d
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None):
+    """O and LSE for q [B,Hq,N,d], k/v [B,Hkv,N,d] (contiguous CUDA tensors)."""
+    B, Hq, Hkv, N, d = _dims(q, k)
+    _check("fa_fwd", load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
+                                   int(causal), float(scale), _dtype_code(q), _stream(stream)))
+
+
+def fa_bwd_workspace_bytes(B: int, Hq: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_bytes(B, Hq, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, workspace, stream=None):
+    B, Hq, Hkv, N, d = _dims(q, k)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fa_bwd", load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
+                                   _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(causal), float(scale),
+                                   _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fa_hadamard_quant_workspace_bytes(rows: int, d: int) -> int:
+    return int(load().fa_hadamard_quant_workspace_bytes(rows, d))
+
+
+def fa_hadamard_quant_fp8(x, signs, x8, descale, workspace, stream=None):
+    d = x.shape[-1]
+    rows = x.numel() // d
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fa_hadamard_quant_fp8", load().fa_hadamard_quant_fp8(
+        _ptr(x), _ptr(signs), _ptr(x8), _ptr(descale), rows, d, _ptr(workspace), ws_bytes,
+        _stream(stream)))
+
+
+def fa_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, o, lse, causal: bool, scale: float,
+               stream=None):
+    B, Hq, Hkv, N, d = _dims(q8, k8)
+    _check("fa_fwd_fp8", load().fa_fwd_fp8(
+        _ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_descale), _ptr(k_descale), _ptr(v_descale), _ptr(o),
+        _ptr(lse), B, Hq, Hkv, N, d, int(causal), float(scale), _stream(stream)))
+
+
+def fa_get_device_status(stream=None) -> int:
+    """FA_OK, or FA_ERR_TIMEOUT if a bounded device wait ran out (clears it)."""
+    return int(load().fa_get_device_status(_stream(stream)))
+
+
+def fa_selftest_bounded_wait(timeout_us: int, stream=None):
+    _check("fa_selftest_bounded_wait", load().fa_selftest_bounded_wait(int(timeout_us), _stream(stream)))

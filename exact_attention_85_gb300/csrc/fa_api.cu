@@ -1,0 +1,221 @@
+// fa_api.cu -- the extern "C" boundary of libfa.so: argument validation,
+// the per-device status word, TMA descriptor encoding and dispatch to the
+// kernel launchers.  Declarations and their contracts are in include/fa.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "host_util.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+// One status word per device that loads the library (module-scope device
+// variable); kernels receive its address as a parameter.
+__device__ unsigned int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned int *g_status_ptr[kMaxDevices];
+std::mutex g_mutex;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+__global__ void selftest_wait_kernel(unsigned int *status, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);  // nothing ever arrives on this barrier
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, (volatile int *)&abort_flag, status, 0xFFFF, limit_ns);
+    __syncthreads();
+}
+
+}  // namespace
+
+bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, uint64_t dim0,
+                  uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {dim0, dim1, dim2};
+    cuuint64_t strides[2] = {dim0 * elem_bytes, dim0 * dim1 * elem_bytes};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    std::memset(map, 0, sizeof(*map));
+    CUresult r = enc(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+unsigned int *device_status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<unsigned int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+cudaError_t launch_selftest_wait(int timeout_us, cudaStream_t st) {
+    unsigned int *status = device_status_ptr();
+    if (!status) return cudaErrorUnknown;
+    selftest_wait_kernel<<<1, 32, 0, st>>>(status, (unsigned long long)timeout_us * 1000ull);
+    return cudaGetLastError();
+}
+
+}  // namespace fa
+
+// ------------------------------------------------------------------ C ABI
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status_t check_shape(int B, int Hq, int Hkv, int N, int d, float scale) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const long long elems = (long long)B * Hq * N * d;
+    if (elems > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
+    // 1-D grid of (Q tiles x heads x batch) CTAs
+    if ((long long)((N + 127) / 128) * B * Hq > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+
+fa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+const char *fa_status_string(fa_status_t s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
+                   int N, int d, int causal, float scale, fa_dtype_t dtype, void *stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
+    if (s != FA_OK) return s;
+    fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_BF16};
+    return from_cuda(fa::launch_fwd(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d) {
+    if (B < 1 || Hq < 1 || N < 1 || d < 1) return 0;
+    const size_t rows = (size_t)B * Hq * N;
+    return round256(rows * sizeof(float)) + round256(rows * (size_t)d * sizeof(float));
+}
+
+fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                   void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                   fa_dtype_t dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
+    if (s != FA_OK) return s;
+    const size_t need = fa_bwd_workspace_bytes(B, Hq, N, d);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FA_ERR_WORKSPACE;
+    const size_t rows = (size_t)B * Hq * N;
+    float *D = static_cast<float *>(workspace);
+    float *dq_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + round256(rows * sizeof(float)));
+    fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_BF16,
+                  D, dq_acc};
+    return from_cuda(fa::launch_bwd(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t fa_hadamard_quant_workspace_bytes(long rows, int d) {
+    (void)rows;
+    (void)d;
+    return 256;
+}
+
+fa_status_t fa_hadamard_quant_fp8(const void *x_bf16, const float *signs, void *x_e4m3, float *descale, long rows,
+                                  int d, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!x_bf16 || !x_e4m3 || !descale || rows < 1) return FA_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(x_e4m3) || (signs && !aligned16(signs))) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if ((long long)rows * d > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < fa_hadamard_quant_workspace_bytes(rows, d) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FA_ERR_WORKSPACE;
+    fa::QuantArgs a{x_bf16, signs, x_e4m3, descale, rows, d, static_cast<float *>(workspace)};
+    return from_cuda(fa::launch_hadamard_quant(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *q_descale,
+                       const float *k_descale, const float *v_descale, void *o_bf16, float *lse, int B, int Hq,
+                       int Hkv, int N, int d, int causal, float scale, void *stream) {
+    if (!q8 || !k8 || !v8 || !q_descale || !k_descale || !v_descale || !o_bf16 || !lse) return FA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q8, k8, v8, o_bf16, lse};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return FA_ERR_INVALID_ARG;
+    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
+    if (s != FA_OK) return s;
+    fa::Fp8FwdArgs a{q8, k8, v8, q_descale, k_descale, v_descale, o_bf16, lse, B, Hq, Hkv, N, d,
+                     causal ? 1 : 0, scale};
+    return from_cuda(fa::launch_fwd_fp8(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status_t fa_get_device_status(void *stream) {
+    unsigned int *p = fa::device_status_ptr();
+    if (!p) return FA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned int host = 0;
+    if (cudaMemcpyAsync(&host, p, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemsetAsync(p, 0, sizeof(unsigned int), st) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+    return (host & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+fa_status_t fa_selftest_bounded_wait(int timeout_us, void *stream) {
+    if (timeout_us < 1 || timeout_us > 1000000) return FA_ERR_INVALID_ARG;
+    return from_cuda(fa::launch_selftest_wait(timeout_us, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// host_util.h -- host-side helpers shared by the launchers: TMA descriptor
+// encoding and the launch-argument structs.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Encodes a 3-D tiled TMA descriptor over a dense [dim2][dim1][dim0] tensor
+// (dim0 contiguous) with a box of box0 x box1 x 1 elements.  Returns false if
+// the driver entry point is unavailable or the encoding is rejected.
+bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                  uint64_t dim0, uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1,
+                  CUtensorMapSwizzle swizzle);
+
+// Device address of this library's status word on the current device.
+unsigned int *device_status_ptr();
+
+struct FwdArgs {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    int B, Hq, Hkv, N, d, causal;
+    float scale;
+    bool bf16;
+};
+
+struct BwdArgs {
+    const void *q, *k, *v, *o, *dO;
+    const float *lse;
+    void *dq, *dk, *dv;
+    int B, Hq, Hkv, N, d, causal;
+    float scale;
+    bool bf16;
+    float *D;      // [B][Hq][N]
+    float *dq_acc; // [B][Hq][N][d]
+};
+
+struct Fp8FwdArgs {
+    const void *q8, *k8, *v8;
+    const float *q_descale, *k_descale, *v_descale;
+    void *o;
+    float *lse;
+    int B, Hq, Hkv, N, d, causal;
+    float scale;
+};
+
+struct QuantArgs {
+    const void *x;
+    const float *signs;
+    void *x8;
+    float *descale;
+    long rows;
+    int d;
+    float *amax;  // workspace cell
+};
+
+cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st);
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st);
+cudaError_t launch_fwd_fp8(const Fp8FwdArgs &a, cudaStream_t st);
+cudaError_t launch_hadamard_quant(const QuantArgs &a, cudaStream_t st);
+cudaError_t launch_selftest_wait(int timeout_us, cudaStream_t st);
+
+}  // namespace fa

@@ -1,0 +1,159 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library libfa.so.
+ *
+ * The operations are those of FlashAttention-2 as described by
+ *   [V2]  "6.2 FlashAttention V2 chi tiet" (infra-guide-du8.pages.dev),
+ *   [CSDN] "FlashAttention-2" algorithm/parallelism article (blog.csdn.net),
+ *   [FA3] "FlashAttention-3: Attention nhanh hon ..." summary (vi.news.hada.io),
+ * with the precise section named at each entry point.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.   Q, O, dO, dQ: [B][Hq][N][d]; K, V, dK, dV: [B][Hkv][N][d]; d is
+ *           contiguous, then N, then head, then batch (dense, no padding).
+ *           LSE: [B][Hq][N] fp32.  Query head h reads key/value head
+ *           h / (Hq / Hkv) (consecutive query heads share a key/value head).
+ * Pointers. All tensor pointers are DEVICE pointers on the current device and
+ *           must be 16-byte aligned.  The caller owns every buffer (inputs,
+ *           outputs, workspace); the library never allocates, frees or
+ *           synchronises device memory, except where an entry point says so.
+ * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  All
+ *           compute entry points are asynchronous on that stream.
+ * Sizes.    1 <= N; d in {64, 128}; Hq % Hkv == 0; B, Hq, Hkv >= 1; the
+ *           element count B*Hq*N*d must fit in 2^31 - 1 per tensor.
+ * Errors.   Invalid arguments are reported before anything is launched
+ *           (FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_WORKSPACE) and
+ *           leave every output untouched.  A failed launch returns
+ *           FA_ERR_CUDA.  Device-side waits are bounded: a wait that runs out
+ *           records FA_ERR_TIMEOUT in a per-device status word (read it with
+ *           fa_get_device_status) and the kernel returns instead of hanging.
+ * Scores.   S = scale * Q K^T; causal masking is top-left aligned (query row r
+ *           sees key c iff c <= r).  LSE is the natural-log log-sum-exp of the
+ *           scaled, masked scores of each row.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, misaligned pointer */
+    FA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d not 64/128) */
+    FA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    FA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    FA_ERR_TIMEOUT = 5        /* a bounded device wait ran out (see status) */
+} fa_status_t;
+
+typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
+
+/*
+ * Forward pass: O = softmax(scale Q K^T [causal mask]) V and LSE.
+ * [V2] section 6.1 (full forward pseudocode: Q-tile outer loop, K/V inner
+ * loop, running max m and sum l, unnormalised O~, single final diag(l)^-1
+ * rescale, L = m + log l); section 5.3 (causal tile classes and early exit);
+ * [CSDN] "parallelism / forward" (one thread block per Q tile x head x batch,
+ * sequence-length parallelism) and 3.1.1 (the recurrence).
+ *   q [B][Hq][N][d], k, v [B][Hkv][N][d]  (in, element type `dtype`)
+ *   o [B][Hq][N][d]                       (out, element type `dtype`)
+ *   lse [B][Hq][N]                        (out, fp32, natural log)
+ */
+fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
+                   float *lse, int B, int Hq, int Hkv, int N, int d,
+                   int causal, float scale, fa_dtype_t dtype, void *stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: D (B*Hq*N fp32, rounded up to 256
+ * bytes) followed by the fp32 dQ accumulator (B*Hq*N*d fp32).
+ */
+size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d);
+
+/*
+ * Backward pass from O, LSE and dO only.
+ * [CSDN] 3.1.2 (step list: D = rowsum(dO o O); per K/V tile j and Q tile i:
+ * S = Q_i K_j^T, P = exp(S - L_i), dV_j += P^T dO_i, dP = dO_i V_j^T,
+ * dS = P o (dP - D_i), dQ_i += dS K_j, dK_j += dS^T Q_i) and "parallelism /
+ * backward" (one thread block per K/V column block, dQ combined across blocks
+ * by atomic addition); [V2] sections 7.1-7.3 (LSE instead of m and l; D
+ * computed once by a separate preprocessing kernel); [CSDN] MQA/GQA paragraph
+ * (dK, dV summed over the query heads of a group).  The scale factor enters
+ * dQ and dK by the chain rule.
+ *   q, k, v, o, lse, dO: as produced/consumed by fa_fwd (in)
+ *   dq [B][Hq][N][d], dk, dv [B][Hkv][N][d]: out, element type `dtype`
+ *   workspace: device buffer of at least fa_bwd_workspace_bytes(B,Hq,N,d)
+ *   bytes, 256-byte aligned; its contents on entry do not matter.
+ * dQ is accumulated with fp32 atomic reductions, so it is deterministic only
+ * up to the order of those additions.
+ */
+fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                   const float *lse, const void *dO, void *dq, void *dk,
+                   void *dv, int B, int Hq, int Hkv, int N, int d, int causal,
+                   float scale, fa_dtype_t dtype, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/*
+ * Bytes of workspace fa_hadamard_quant_fp8 needs (the fp32 amax cell).
+ */
+size_t fa_hadamard_quant_workspace_bytes(long rows, int d);
+
+/*
+ * Incoherent processing + per-tensor e4m3 quantisation of one tensor.
+ * [FA3] "FP8 and incoherent processing": multiply by a random orthogonal
+ * matrix, realised as a Hadamard transform with random signs, O(d log d) per
+ * row; here x' = (x o s) H_d / sqrt(d) for every row of d values, then
+ * sigma = amax(|x'|) / 448 over the whole tensor and x8 = e4m3(x' / sigma)
+ * (round to nearest even, saturating).
+ *   x_bf16  [rows][d] bf16 (in)
+ *   signs   [d] fp32 of +-1 (in), or NULL for no rotation (plain FP8)
+ *   x_e4m3  [rows][d] e4m3 (out)
+ *   descale one fp32 device scalar (out): sigma, so x' ~= sigma * x8
+ *   workspace: >= fa_hadamard_quant_workspace_bytes(rows, d) bytes
+ * d must be 64 or 128.
+ */
+fa_status_t fa_hadamard_quant_fp8(const void *x_bf16, const float *signs,
+                                  void *x_e4m3, float *descale, long rows,
+                                  int d, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
+ * FP8 (e4m3) forward: the fa_fwd algorithm on e4m3 Q, K, V with fp32
+ * descales (device scalars), producing bf16 O and fp32 LSE of the
+ * *dequantised* scores: S = scale * q_descale * k_descale * Q8 K8^T,
+ * O = softmax(S) (v_descale * V8).
+ * [FA3] "FP8" (tensor-core throughput doubles at 8 bits) and the FP8 forward
+ * figures of that page.  Q and K may have been rotated by the same random-sign
+ * Hadamard matrix, which leaves Q K^T unchanged.
+ */
+fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8,
+                       const float *q_descale, const float *k_descale,
+                       const float *v_descale, void *o_bf16, float *lse,
+                       int B, int Hq, int Hkv, int N, int d, int causal,
+                       float scale, void *stream);
+
+/*
+ * Reads and clears the current device's status word, which kernels set when
+ * a bounded wait runs out.  Synchronises `stream` first.  Returns FA_OK or
+ * FA_ERR_TIMEOUT (or FA_ERR_CUDA if the copy itself fails).
+ */
+fa_status_t fa_get_device_status(void *stream);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one block that waits on a
+ * barrier nothing will ever complete, with a limit of `timeout_us`
+ * microseconds (1 .. 1000000).  The wait runs out, the kernel records
+ * FA_ERR_TIMEOUT in the status word and returns; nothing faults or hangs.
+ */
+fa_status_t fa_selftest_bounded_wait(int timeout_us, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *fa_status_string(fa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */
