@@ -1,0 +1,379 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = the whole path once over one batch of synthetic input: the
+forward (fa_fwd) and the backward (fa_bwd: D preprocessing, the K/V-tile
+main kernel, dQ conversion) at the headline shape B=4, H=16, N=8192, d=128,
+bf16, causal.  The metric is attention TFLOPS, counting 4 B H N^2 d for the
+forward (halved for causal) and 2.5x that for the backward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle (test infrastructure, the
+only other place this script runs it) on a bounded sample of the same
+workload.  Under torchrun (N > 1) every rank processes its own batch shard
+(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS on 1 GB300 (bf16 d=128 N=8K causal); % of tensor peak"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None, help="workload name (default: the headline shape)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"bf16_tflops": p["bf16_tflops"], "bf16_tflops_sustained": p["bf16_tflops_sustained"],
+                "hbm_gbs": p["hbm_gbs"], "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+def _src_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "exact_attention_85_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str, files):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel
+    source is unchanged since that capture; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)[kernel]
+    except Exception:
+        return None
+    return t["bytes_per_launch"] if t.get("src_sha") == _src_sha(files) else None
+
+
+class ClockSampler:
+    """nvidia-smi samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        loaded = [r for r in rows if r[2] > 300.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(loaded)}
+
+
+def run_ours(a):
+    import torch
+
+    from exact_attention_85_gb300 import _lib, attention_bwd, attention_fwd
+    from exact_attention_85_gb300.inputs import HEADLINE, WORKLOADS, make_inputs
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[a.workload or HEADLINE]
+    lib = _lib.load()
+    stream = torch.cuda.current_stream()
+
+    # each rank owns its own batch shard (seeded by rank): weak scaling
+    host = make_inputs(w, seed=w.seed + 1000 * rank, with_grad=True)
+    q, k, v, dO = (host[n].to(dev).contiguous() for n in ("q", "k", "v", "dO"))
+    B, Hq, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = _lib.fa_bwd_workspace_bytes(B, Hq, N, d)
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def fwd():
+        _lib.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+
+    def bwd():
+        _lib.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, w.causal, w.scale, workspace, stream)
+
+    has_bwd = w.backward
+    if has_bwd:
+        fwd()
+        try:
+            bwd()
+        except _lib.FAError as e:  # a build without the backward kernels
+            if e.status != _lib.FA_ERR_CUDA:
+                raise
+            has_bwd = False
+    for _ in range(a.warmup):
+        fwd()
+        if has_bwd:
+            bwd()
+        flush.zero_()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    launches = 0
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(a.steps):
+            ev[i][0].record(stream)
+            fwd()
+            launches += 1
+            ev[i][1].record(stream)
+            if has_bwd:
+                bwd()
+                launches += 3
+            ev[i][2].record(stream)
+            flush.zero_()  # L2 flush between steps, outside the events
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if ws > 1:
+        torch.distributed.barrier()
+    status = _lib.fa_get_device_status(stream)
+    if status != _lib.FA_OK:
+        raise RuntimeError("a bounded device wait ran out during the timed region")
+
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev] if has_bwd else [0.0] * a.steps
+    step_ms = statistics.mean(f + b for f, b in zip(fwd_ms, bwd_ms))
+    if ws > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    f_fwd = w.fwd_flops()
+    f_bwd = w.bwd_flops() if has_bwd else 0.0
+    value = ws * (f_fwd + f_bwd) / (step_ms * 1e-3) / 1e12
+    peaks = _peaks()
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_avg = statistics.mean(bwd_ms) if has_bwd else 0.0
+    fwd_tf = f_fwd / (fwd_avg * 1e-3) / 1e12
+    bwd_tf = f_bwd / (bwd_avg * 1e-3) / 1e12 if has_bwd else None
+
+    # roofline of the dominant kernel (the longer of the two timed calls)
+    if has_bwd and bwd_avg > fwd_avg:
+        dom, dom_ms, dom_flops = "fa_bwd (main kernel; duration includes the small D and dQ-convert kernels)", bwd_avg, f_bwd
+        traffic = _traffic("bwd_kernel", ["fa_bwd.cu"])
+    else:
+        dom, dom_ms, dom_flops = "fwd_kernel", fwd_avg, f_fwd
+        traffic = _traffic("fwd_kernel", ["fa_fwd.cu"])
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
+            "peak_source": f"{peaks['source']} bf16 burst (kernel timed alone with CUDA events)"}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "TFLOPS", "n_gpus": ws, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                   "causal": w.causal, "per_gpu_batch": w.B, "global_batch": w.B * ws,
+                   "parallelism": f"dp{ws} (batch shards, no collective)",
+                   "l2": "flushed between steps (256 MB write); inputs 537 MB also exceed L2",
+                   "backward_included": has_bwd},
+        "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
+        "fwd_tflops": round(fwd_tf, 1), "bwd_tflops": None if bwd_tf is None else round(bwd_tf, 1),
+        "fwd_frac_of_peak": round(fwd_tf / peaks["bf16_tflops"], 4),
+        "bwd_frac_of_peak": None if bwd_tf is None else round(bwd_tf / peaks["bf16_tflops"], 4),
+        "roofline": roof, "gpu_launches": launches, "wall_s_timed": round(wall, 3),
+        "clocks": clk.summary(),
+    }
+
+    if not a.no_e2e:
+        result["e2e"] = _e2e(a, w, host, dev, stream, has_bwd, ws)
+    if rank == 0 and ws == 1 and not a.no_cpu:
+        result["cpu_baseline"] = _cpu_baseline(w, host, budget_s=12.0)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _e2e(a, w, host, dev, stream, has_bwd, ws):
+    """Same metric through the public API with pinned host buffers: every step
+    copies Q, K, V, dO in and O, dQ, dK, dV out inside the timed region."""
+    import torch
+
+    from exact_attention_85_gb300 import attention_bwd, attention_fwd
+
+    names_in = ("q", "k", "v", "dO")
+    h_in = {n: host[n].pin_memory() for n in names_in}
+    h_out = {n: torch.empty_like(host["q" if n in ("o", "dq") else "k"]).pin_memory()
+             for n in (("o", "dq", "dk", "dv") if has_bwd else ("o",))}
+    steps = max(3, min(a.steps, 10))
+
+    def step():
+        d_in = {n: h_in[n].to(dev, non_blocking=True) for n in names_in}
+        o, lse = attention_fwd(d_in["q"], d_in["k"], d_in["v"], w.causal, w.scale)
+        outs = {"o": o}
+        if has_bwd:
+            dq, dk, dv = attention_bwd(d_in["q"], d_in["k"], d_in["v"], o, lse, d_in["dO"], w.causal, w.scale)
+            outs.update(dq=dq, dk=dk, dv=dv)
+        for n, t in outs.items():
+            h_out[n].copy_(t, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    flops = w.fwd_flops() + (w.bwd_flops() if has_bwd else 0.0)
+    h2d = sum(h_in[n].numel() * h_in[n].element_size() for n in names_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    return {"value": round(ws * flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOPS", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def _cpu_sample(w, host, n_groups: int):
+    """fp64 oracle forward + backward of the first `n_groups` (batch, kv-head)
+    groups at full sequence length; returns (seconds, algorithmic flops)."""
+    import oracle
+
+    G = w.Hq // w.Hkv
+    t0 = time.perf_counter()
+    done = 0
+    for idx in range(n_groups):
+        b, g = divmod(idx, w.Hkv)
+        sl_q = slice(g * G, g * G + G)
+        oracle.attention_bwd_group(host["q"][b:b + 1, sl_q], host["k"][b:b + 1, g:g + 1],
+                                   host["v"][b:b + 1, g:g + 1], host["dO"][b:b + 1, sl_q],
+                                   0, 0, w.causal, w.scale)
+        done += G
+    secs = time.perf_counter() - t0
+    per_head = (w.fwd_flops() + w.bwd_flops()) / (w.B * w.Hq)
+    return secs, per_head * done
+
+
+def _cpu_baseline(w, host, budget_s: float):
+    threads = os.cpu_count() or 1
+    secs, flops = _cpu_sample(w, host, 1)
+    n = 1
+    if secs < budget_s / 2:
+        extra = max(0, int(budget_s / max(secs, 1e-3)) - 1)
+        if extra:
+            s2, f2 = _cpu_sample(w, host, min(extra, w.B * w.Hkv))
+            secs, flops, n = secs + s2, flops + f2, 1 + min(extra, w.B * w.Hkv)
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 oracle forward+backward of {n} (batch, kv-head) group(s) of {w.name} at full "
+                      f"N={w.N}, {secs:.1f} s, OpenMP over {threads} host threads"}
+
+
+def run_reference(a):
+    """The fp64 CPU oracle as the reference arm (rank 0 only)."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from exact_attention_85_gb300.inputs import HEADLINE, WORKLOADS, make_inputs
+    w = WORKLOADS[a.workload or HEADLINE]
+    host = make_inputs(w, with_grad=True)
+    threads = os.cpu_count() or 1
+    for _ in range(a.warmup):
+        _cpu_sample(w, host, 1)
+    times, flops = [], 0.0
+    for i in range(a.steps):
+        s, f = _cpu_sample(w, host, 1)
+        times.append(s)
+        flops = f
+    ms = statistics.mean(times) * 1e3
+    value = flops / (ms * 1e-3) / 1e12
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS", "n_gpus": ws,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+                   "causal": w.causal, "sample_per_step": "one (batch, kv-head) group at full N"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": "each step: fp64 oracle forward+backward of one (batch, kv-head) group at "
+                                   f"full N={w.N}"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)

@@ -228,13 +228,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         const float sl2 = p.scale_log2;
         float m_ref = -INFINITY;
-        float l_sum = 0.0f;
+        float l_sum = 0.0f;    // sum of the rounded P fed to the MMA: normalises O
+        float l_exact = 0.0f;  // sum of the unrounded P: gives L
         bool ok = true;
         uint32_t s[128];
 
         for (int j = 0; j < nkv; ++j) {
             const int sb = j & 1;
-            if (!mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.status, 7)) { ok = false; break; }
+            // every lane waits, then the warp votes: the tcgen05.ld/st below
+            // are warp-collective (.sync.aligned) and need all 32 lanes
+            const bool got_s = mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.status, 7);
+            if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
             tc_fence_after();
             const uint32_t s_addr = lane_base + kColS + sb * kBN;
             tmem_ld_x32(s_addr + 0, s + 0);
@@ -269,11 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (mx > m_ref + kRescaleThreshold) {
                 alpha = ex2_approx(m_ref - mx);  // 0 on the first tile (m_ref = -inf)
                 l_sum *= alpha;
+                l_exact *= alpha;
                 m_ref = mx;
                 rescale = true;
             }
             const float neg_m = -m_ref;
-            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f, e0 = 0.f, e1 = 0.f;
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
@@ -281,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, neg_m));
                 const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), sl2, neg_m));
                 const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), sl2, neg_m));
-                l0 += p0; l1 += p1; l2 += p2; l3 += p3;
+                // l sums the rounded P that the MMA consumes, so O~ / l is an
+                // exactly normalised mix of V rows even when one term dominates
                 if constexpr (BF16) {
                     pk[c / 2] = pack_bf16x2(p0, p1);
                     pk[c / 2 + 1] = pack_bf16x2(p2, p3);
@@ -289,16 +295,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[c / 2] = pack_f16x2(p0, p1);
                     pk[c / 2 + 1] = pack_f16x2(p2, p3);
                 }
+                const float2 r01 = unpack2<BF16>(pk[c / 2]);
+                const float2 r23 = unpack2<BF16>(pk[c / 2 + 1]);
+                l0 += r01.x; l1 += r01.y; l2 += r23.x; l3 += r23.y;
+                e0 += p0 + p1; e1 += p2 + p3;
             }
             l_sum += (l0 + l1) + (l2 + l3);
+            l_exact += e0 + e1;
+            __syncwarp();  // reconverge after the per-row branches above
             const uint32_t p_addr = lane_base + kColP + sb * 64;
             tmem_st_x32(p_addr, pk);
             tmem_st_x32(p_addr + 32, pk + 32);
 
             if (j >= 1) {
                 // O holds P_0..P_{j-1} contributions once PV_{j-1} completes
-                if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status, 8)) { ok = false; break; }
-                if (rescale) {
+                const bool got_o = mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status, 8);
+                if (!__all_sync(0xffffffffu, got_o)) { ok = false; break; }
+                // warp-uniform branch; lanes that keep their max use alpha = 1
+                if (__any_sync(0xffffffffu, rescale)) {
                     tc_fence_after();
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -317,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         if (ok && nkv > 0) ok = mbar_wait(o_done, (nkv - 1) & 1, abort_flag, p.status, 9);
+        __syncwarp();
         // uniform decision across the 128 softmax threads (the epilogue has a
         // named barrier that all of them must reach)
         ok = named_bar_and(1, kBM, ok);
@@ -356,8 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_wait_read_all();
             }
             if (q0 + row < p.N)
-                p.lse[(size_t)q_plane * p.N + q0 + row] = (m_ref + log2f(l_sum)) * 0.69314718055994530942f;
+                p.lse[(size_t)q_plane * p.N + q0 + row] = (m_ref + log2f(l_exact)) * 0.69314718055994530942f;
         }
+        __syncwarp();
     }
 
     tc_fence_before();

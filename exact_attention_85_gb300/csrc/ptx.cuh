@@ -329,4 +329,19 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return r;
 }
 
+// Widens a packed 16-bit pair (lo in bits 0-15) back to two floats.
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+    if constexpr (BF16) {
+        return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+    } else {
+        float lo, hi;
+        asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}\n"
+            : "=f"(lo), "=f"(hi)
+            : "r"(v));
+        return make_float2(lo, hi);
+    }
+}
+
 }  // namespace fa
