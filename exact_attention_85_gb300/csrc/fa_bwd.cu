@@ -1,4 +1,581 @@
+// fa_bwd.cu -- FlashAttention-2 backward for sm_103a (bf16 / fp16, d = 64, 128).
+//
+// Algorithm (blog.csdn.net FlashAttention-2 article, 3.1.2 and "parallelism /
+// backward"; "6.2 FlashAttention V2 chi tiet", section 7): only L and
+// D = rowsum(dO o O) are used; D comes from a separate preprocessing kernel;
+// one CTA owns a K/V column block j and walks every Q tile i, recomputing
+// S = Q_i K_j^T and P = exp(S - L_i), accumulating dV_j += P^T dO_i and
+// dK_j += dS^T Q_i on chip, and adding dQ_i += dS K_j into an fp32 dQ
+// accumulator shared by all CTAs (atomic addition).  Grouped-query heads: the
+// CTA of key/value head g walks the Q tiles of all query heads of its group,
+// so dK/dV are summed over the group before they are stored (MQA/GQA
+// paragraph of the blog.csdn.net page).
+//
+// Kernels:
+//   bwd_pre_kernel   D = rowsum(dO o O) (fp32) and dQacc = 0     (HBM bound)
+//   bwd_main_kernel  the K/V-tile loop below                     (tensor bound)
+//   bwd_dq_kernel    dQ = scale * dQacc, converted to the element type
+//
+// Main kernel, one CTA per (128-key tile, key/value head, batch); Q tiles of
+// 64 rows.  Tensor memory (512 columns, fp32, lane = key row unless noted):
+//   buffer b (b = 0, 1; base 128 b):
+//     [0, 64)   S^T = K_j Q_i^T       -> then [0, 32) P^T, [32, 64) dS^T (16-bit pairs)
+//     [64, 128) dP^T = V_j dO_i^T     -> then dQ_i^T = K_j^T dS_i^T (lane = head-dim index)
+//   [256, 256 + d) dV_j,  [384, 384 + d) dK_j  (accumulated over all Q tiles)
+// P^T and dS^T stay in tensor memory as the A operands of dV += P^T dO and
+// dK += dS^T Q; dS^T is also written to shared memory as the B operand of
+// dQ^T = K^T dS^T.  dQ^T is read out by four warps and added into dQacc with
+// fp32 atomic reductions (one 128-byte line per warp and query row).
+// Warps: 0-3 and 10-13 softmax (P, dS; warps 0-3 then store dV), 4 TMA
+// producer, 5 MMA issuer + TMEM owner, 6-9 dQ read-out (then store dK).
+// Q / dO tiles stream through a 3-deep ring so their loads are issued two
+// tiles ahead of use.
 #include "host_util.h"
+#include "ptx.cuh"
+
 namespace fa {
-cudaError_t launch_bwd(const BwdArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+
+namespace {
+
+constexpr int kBQ = 64;        // query rows per Q tile
+constexpr int kBKV = 128;      // key rows per CTA (TMEM lanes)
+constexpr int kThreads = 448;  // 14 warps
+constexpr int kSoftmaxThreads = 256;
+
+template <int D>
+struct BwdLayout {
+    static constexpr int NBOX = D / 64;
+    static constexpr int TILE_KV = kBKV * D * 2;  // K or V tile, bytes
+    static constexpr int TILE_Q = kBQ * D * 2;    // Q or dO tile
+    static constexpr int BOX_KV = kBKV * 128;     // one 64-column box of a K/V tile
+    static constexpr int BOX_Q = kBQ * 128;       // one 64-column box of a Q/dO tile
+    static constexpr int QS = 3;                  // Q/dO ring depth
+    static constexpr int DS_BYTES = kBKV * kBQ * 2;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + TILE_KV;
+    static constexpr int OFF_QD = OFF_V + TILE_KV;  // stage s: Q at +2s*TILE_Q, dO at +(2s+1)*TILE_Q
+    static constexpr int OFF_DS = OFF_QD + QS * 2 * TILE_Q;
+    static constexpr int OFF_LD = OFF_DS + 2 * DS_BYTES;  // stage s: L2[64], D[64]
+    static constexpr int OFF_BAR = OFF_LD + QS * 2 * kBQ * 4;
+    // kv_full, qd_full[QS], qd_empty[QS], sdp_full[2], ds_ready[2], dq_full[2],
+    // dq_free[2], acc_done, drain
+    static constexpr int NBAR = 1 + 2 * QS + 2 * 4 + 2;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int ALLOC = BYTES + 1024;
+    // the dV / dK epilogue stages each 128 x d output tile in one Q/dO stage
+    static_assert(2 * TILE_Q >= TILE_KV, "an output tile must fit in one Q/dO stage");
+};
+
+struct BwdParams {
+    const float *lse;
+    const float *Dvec;
+    float *dq_acc;
+    unsigned int *status;
+    int Hq, Hkv, N, nkv, nq;
+    int causal;
+    float scale, scale_log2;
+};
+
+constexpr uint32_t kColDV = 256, kColDK = 384;
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                    const BwdParams p) {
+    using L = BwdLayout<D>;
+    constexpr int QS = L::QS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint64_t *kv_full = bars;
+    uint64_t *qd_full = bars + 1;
+    uint64_t *qd_empty = qd_full + QS;
+    uint64_t *sdp_full = qd_empty + QS;
+    uint64_t *ds_ready = sdp_full + 2;
+    uint64_t *dq_full = ds_ready + 2;
+    uint64_t *dq_free = dq_full + 2;
+    uint64_t *acc_done = dq_free + 2;
+    uint64_t *drain = acc_done + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+    float *ld_smem = reinterpret_cast<float *>(smem + L::OFF_LD);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const int bg = blockIdx.x / p.nkv;  // batch * Hkv + g
+    const int jt = blockIdx.x - bg * p.nkv;
+    const int b = bg / p.Hkv;
+    const int g = bg - b * p.Hkv;
+    const int G = p.Hq / p.Hkv;
+    const int kv0 = jt * kBKV;
+    const int i_start = p.causal ? 2 * jt : 0;  // first Q tile with a row >= kv0
+    const int n_i = p.nq - i_start;
+    const int n_it = G * n_i;
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        for (int s = 0; s < QS; ++s) {
+            // 1 arrival with the expected transaction bytes (lane 0, before the
+            // copies) + 32 arrivals after the lanes have written L and D
+            mbar_init(&qd_full[s], 33);
+            mbar_init(&qd_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sdp_full[s], 1);
+            mbar_init(&ds_ready[s], kSoftmaxThreads);
+            mbar_init(&dq_full[s], 1);
+            mbar_init(&dq_free[s], 128);
+        }
+        mbar_init(acc_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto q_stage = [&](int st) { return smem + L::OFF_QD + (2 * st) * L::TILE_Q; };
+    auto do_stage = [&](int st) { return smem + L::OFF_QD + (2 * st + 1) * L::TILE_Q; };
+
+    if (warp == 4) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(kv_full, 2 * L::TILE_KV);
+            for (int bx = 0; bx < L::NBOX; ++bx) {
+                tma_load_3d(smem + L::OFF_K + bx * L::BOX_KV, &tm_k, kv_full, bx * 64, kv0, bg);
+                tma_load_3d(smem + L::OFF_V + bx * L::BOX_KV, &tm_v, kv_full, bx * 64, kv0, bg);
+            }
+        }
+        int it = 0;
+        for (; it < n_it; ++it) {
+            const int st = it % QS;
+            bool ok = true;
+            if (lane == 0 && it >= QS)
+                ok = mbar_wait(&qd_empty[st], ((it / QS) + 1) & 1, abort_flag, p.status, 21);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            const int h = g * G + it / n_i;
+            const int q_base = (i_start + it % n_i) * kBQ;
+            const int plane = b * p.Hq + h;
+            if (lane == 0) {
+                // tensor copies first, so their latency overlaps the L / D loads
+                mbar_arrive_expect_tx(&qd_full[st], 2 * L::TILE_Q);
+                for (int bx = 0; bx < L::NBOX; ++bx) {
+                    tma_load_3d(q_stage(st) + bx * L::BOX_Q, &tm_q, &qd_full[st], bx * 64, q_base, plane);
+                    tma_load_3d(do_stage(st) + bx * L::BOX_Q, &tm_do, &qd_full[st], bx * 64, q_base, plane);
+                }
+            }
+            float *l2s = ld_smem + st * 2 * kBQ;
+            float *dsm = l2s + kBQ;
+            for (int r = lane; r < kBQ; r += 32) {
+                const int row = q_base + r;
+                const bool in = row < p.N;
+                // rows past N: L = +inf makes P = 0 for them
+                l2s[r] = in ? p.lse[(size_t)plane * p.N + row] * 1.4426950408889634f : INFINITY;
+                dsm[r] = in ? p.Dvec[(size_t)plane * p.N + row] : 0.0f;
+            }
+            mbar_arrive(&qd_full[st]);  // releases this lane's L / D writes
+        }
+        if (lane == 0 && *abort_flag) {
+            // let copies already in flight land before the CTA exits
+            mbar_wait_drain(kv_full, 0, 10000000ull);
+            for (int t = max(0, it - QS); t < it; ++t)
+                mbar_wait_drain(&qd_full[t % QS], (t / QS) & 1, 10000000ull);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t fmt = BF16 ? 1u : 0u;
+            constexpr uint32_t idesc_sdp = make_idesc(kBKV, kBQ, fmt, false, false);  // K-major both
+            constexpr uint32_t idesc_acc = make_idesc(kBKV, D, fmt, false, true);     // A tmem, B MN-major
+            constexpr uint32_t idesc_dq = make_idesc(kBKV, kBQ, fmt, true, true);     // A, B MN-major
+            const uint32_t k_addr = smem_u32(smem + L::OFF_K);
+            const uint32_t v_addr = smem_u32(smem + L::OFF_V);
+            bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 22);
+
+            // S^T = K_j Q_t^T and dP^T = V_j dO_t^T into tensor-memory buffer t % 2
+            auto issue_sdp = [&](int t) -> bool {
+                const int bb = t & 1;
+                const int st = t % QS;
+                if (!mbar_wait(&qd_full[st], (t / QS) & 1, abort_flag, p.status, 23)) return false;
+                tc_fence_after();
+                const uint32_t q_addr = smem_u32(q_stage(st));
+                const uint32_t do_addr = smem_u32(do_stage(st));
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
+                    const uint32_t oq = (kk >> 2) * L::BOX_Q + (kk & 3) * 32;
+                    mma_f16_ss(tmem + bb * 128, make_sdesc_sw128(k_addr + okv, 16, 1024),
+                               make_sdesc_sw128(q_addr + oq, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
+                    const uint32_t oq = (kk >> 2) * L::BOX_Q + (kk & 3) * 32;
+                    mma_f16_ss(tmem + bb * 128 + 64, make_sdesc_sw128(v_addr + okv, 16, 1024),
+                               make_sdesc_sw128(do_addr + oq, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&sdp_full[bb]);
+                return true;
+            };
+
+            if (ok) ok = issue_sdp(0);
+            if (ok && n_it > 1) ok = issue_sdp(1);
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int bb = it & 1;
+                const int st = it % QS;
+                if (!mbar_wait(&ds_ready[bb], (it >> 1) & 1, abort_flag, p.status, 24)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t ds_addr = smem_u32(smem + L::OFF_DS + bb * L::DS_BYTES);
+                // dQ_i^T = K_j^T dS_i^T: A = K^T (head dim contiguous: MN-major), B = dS^T
+                // rows of keys in shared memory (MN-major).  For d = 64 the second
+                // 64-row half of A repeats the first (LBO 0); those rows are unused.
+#pragma unroll
+                for (int kk = 0; kk < kBKV / 16; ++kk)
+                    mma_f16_ss(tmem + bb * 128 + 64,
+                               make_sdesc_sw128(k_addr + kk * 2048, D == 128 ? L::BOX_KV : 0, 1024),
+                               make_sdesc_sw128(ds_addr + kk * 2048, 0, 1024), idesc_dq, kk > 0 ? 1u : 0u);
+                mma_commit(&dq_full[bb]);
+                const uint32_t q_addr = smem_u32(q_stage(st));
+                const uint32_t do_addr = smem_u32(do_stage(st));
+                // dV_j += P^T dO_i and dK_j += dS^T Q_i (A from tensor memory)
+#pragma unroll
+                for (int kk = 0; kk < kBQ / 16; ++kk)
+                    mma_f16_ts(tmem + kColDV, tmem + bb * 128 + kk * 8,
+                               make_sdesc_sw128(do_addr + kk * 2048, L::BOX_Q, 1024), idesc_acc,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < kBQ / 16; ++kk)
+                    mma_f16_ts(tmem + kColDK, tmem + bb * 128 + 32 + kk * 8,
+                               make_sdesc_sw128(q_addr + kk * 2048, L::BOX_Q, 1024), idesc_acc,
+                               (it > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&qd_empty[st]);
+                if (it + 2 < n_it) {
+                    // buffer bb is reused once dQ_i^T has been read out of it
+                    if (!mbar_wait(&dq_free[bb], (it >> 1) & 1, abort_flag, p.status, 25)) { ok = false; break; }
+                    tc_fence_after();
+                    if (!issue_sdp(it + 2)) { ok = false; break; }
+                }
+            }
+            if (ok) mma_commit(acc_done);
+            // every MMA issued above has completed once `drain` flips
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0, 100000000ull);
+        }
+        __syncwarp();
+    } else if (warp < 4 || warp >= 10) {
+        // ------------------------------------------- softmax: P^T and dS^T
+        // Eight warps: warp w covers key rows 32 (w % 4) .. + 31 (its TMEM
+        // lane quarter) and query columns 32 hf .. + 31 of the Q tile.
+        const int hf = warp < 4 ? 0 : 1;
+        const int quarter = warp & 3;
+        const int c = quarter * 32 + lane;  // key row within the tile == TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const float sl2 = p.scale_log2;
+        const int kv = kv0 + c;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int bb = it & 1;
+            const int st = it % QS;
+            // every lane waits, then the warp votes: the tcgen05.ld/st below
+            // are warp-collective and need all 32 lanes
+            const bool w1 = mbar_wait(&sdp_full[bb], (it >> 1) & 1, abort_flag, p.status, 26);
+            const bool w2 = w1 && mbar_wait(&qd_full[st], (it / QS) & 1, abort_flag, p.status, 27);
+            if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t s[32], dp[32];
+            tmem_ld_x32(lane_base + bb * 128 + hf * 32, s);
+            tmem_ld_x32(lane_base + bb * 128 + 64 + hf * 32, dp);
+            tmem_ld_wait_x32(s);
+            tmem_ld_wait_x32(dp);
+            const float *l2s = ld_smem + st * 2 * kBQ + hf * 32;
+            const float *dsm = ld_smem + st * 2 * kBQ + kBQ + hf * 32;
+            const int q_first = (i_start + it % n_i) * kBQ + hf * 32;
+            const bool diag = p.causal && (q_first < kv0 + kBKV);
+            uint32_t pp[16], dd[16];
+#pragma unroll
+            for (int r = 0; r < 32; r += 2) {
+                const float2 lv = *reinterpret_cast<const float2 *>(l2s + r);
+                const float2 dv = *reinterpret_cast<const float2 *>(dsm + r);
+                float p0 = ex2_approx(fmaf(__uint_as_float(s[r]), sl2, -lv.x));
+                float p1 = ex2_approx(fmaf(__uint_as_float(s[r + 1]), sl2, -lv.y));
+                if (diag) {  // causal: key kv is visible to query q iff kv <= q
+                    if (kv > q_first + r) p0 = 0.0f;
+                    if (kv > q_first + r + 1) p1 = 0.0f;
+                }
+                const float d0 = p0 * (__uint_as_float(dp[r]) - dv.x);
+                const float d1 = p1 * (__uint_as_float(dp[r + 1]) - dv.y);
+                if constexpr (BF16) {
+                    pp[r / 2] = pack_bf16x2(p0, p1);
+                    dd[r / 2] = pack_bf16x2(d0, d1);
+                } else {
+                    pp[r / 2] = pack_f16x2(p0, p1);
+                    dd[r / 2] = pack_f16x2(d0, d1);
+                }
+            }
+            __syncwarp();
+            tmem_st_x16(lane_base + bb * 128 + hf * 16, pp);
+            tmem_st_x16(lane_base + bb * 128 + 32 + hf * 16, dd);
+            // dS^T row c, query columns 32 hf .. + 31 -> shared memory (the
+            // 128-byte swizzled row of 64 values; this warp writes chunks 4 hf .. + 3)
+            uint8_t *row = smem + L::OFF_DS + bb * L::DS_BYTES + c * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4 *>(row + (((4 * hf + q) ^ (c & 7)) << 4)) =
+                    make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+            fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&ds_ready[bb]);
+        }
+        // ------------------------------------------------- dV epilogue
+        if (warp < 4) {
+            bool ok2 = ok && mbar_wait(acc_done, 0, abort_flag, p.status, 28);
+            __syncwarp();
+            ok2 = named_bar_and(1, 128, ok2);
+            if (ok2) {
+                tc_fence_after();
+                uint8_t *stage = q_stage(0);  // idle after the last MMA
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld_x32(lane_base + kColDV + c0, o);
+                    tmem_ld_wait_x32(o);
+                    uint32_t wv[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x)
+                        wv[x] = BF16 ? pack_bf16x2(__uint_as_float(o[2 * x]), __uint_as_float(o[2 * x + 1]))
+                                     : pack_f16x2(__uint_as_float(o[2 * x]), __uint_as_float(o[2 * x + 1]));
+                    uint8_t *rowp = stage + (c0 >> 6) * L::BOX_KV + c * 128;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int chunk = ((c0 & 63) >> 3) + q;
+                        *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (c & 7)) << 4)) =
+                            make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                if (c == 0) {
+                    for (int bx = 0; bx < L::NBOX; ++bx)
+                        tma_store_3d(&tm_dv, stage + bx * L::BOX_KV, bx * 64, kv0, bg);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------- dQ read-out and atomic reduction
+        // warps 6..9: thread t = TMEM lane = head-dim index of dQ^T
+        const int t = (warp & 3) * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+            const int bb = it & 1;
+            const bool got = mbar_wait(&dq_full[bb], (it >> 1) & 1, abort_flag, p.status, 29);
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t v[64];
+            tmem_ld_x32(lane_base + bb * 128 + 64, v);
+            tmem_ld_x32(lane_base + bb * 128 + 96, v + 32);
+            tmem_ld_wait_x32(v);
+            tmem_ld_wait_x32(v + 32);
+            tc_fence_before();
+            mbar_arrive(&dq_free[bb]);
+            const int h = g * G + it / n_i;
+            const int q_base = (i_start + it % n_i) * kBQ;
+            const int rows = min(kBQ, p.N - q_base);
+            if (t < D) {
+                // element (q_base + r, t) of this head's dQ: consecutive lanes
+                // touch consecutive floats (one 128-byte line per warp and row)
+                float *dst = p.dq_acc + ((size_t)(b * p.Hq + h) * p.N + q_base) * D + t;
+#pragma unroll
+                for (int r = 0; r < kBQ; ++r)
+                    if (r < rows) atomicAdd(dst + (size_t)r * D, __uint_as_float(v[r]));
+            }
+        }
+        // ------------------------------------------------- dK epilogue
+        bool ok2 = ok && mbar_wait(acc_done, 0, abort_flag, p.status, 30);
+        __syncwarp();
+        ok2 = named_bar_and(2, 128, ok2);
+        if (ok2) {
+            tc_fence_after();
+            uint8_t *stage = q_stage(1);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld_x32(lane_base + kColDK + c0, o);
+                tmem_ld_wait_x32(o);
+                uint32_t wk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const float a0 = __uint_as_float(o[2 * x]) * p.scale;
+                    const float a1 = __uint_as_float(o[2 * x + 1]) * p.scale;
+                    wk[x] = BF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
+                }
+                uint8_t *rowp = stage + (c0 >> 6) * L::BOX_KV + t * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = ((c0 & 63) >> 3) + q;
+                    *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (t & 7)) << 4)) =
+                        make_uint4(wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(2, 128);
+            if (t == 0) {
+                for (int bx = 0; bx < L::NBOX; ++bx)
+                    tma_store_3d(&tm_dk, stage + bx * L::BOX_KV, bx * 64, kv0, bg);
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
 }
+
+// D[row] = sum_c dO[row, c] * O[row, c]; also zeroes the fp32 dQ accumulator.
+// 16 lanes per row, 16-byte loads.
+template <bool BF16>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4 *__restrict__ o, const uint4 *__restrict__ dO,
+                                                      float *__restrict__ Dvec, float4 *__restrict__ dq_acc,
+                                                      long rows, int d, long acc_vec4) {
+    const long tid = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long nthreads = (long)gridDim.x * blockDim.x;
+    const int vec_per_row = d / 8;  // 8 elements per uint4
+    // each warp takes two rows per trip (16 lanes each); the trip count is
+    // uniform across the warp so the full-mask shuffles below are convergent
+    const long warp_id = tid >> 5;
+    const long nwarps = nthreads >> 5;
+    const int half = (threadIdx.x >> 4) & 1;
+    const int sub = threadIdx.x & 15;
+    for (long base = warp_id * 2; base < rows; base += nwarps * 2) {
+        const long row = base + half;
+        float acc = 0.0f;
+        if (row < rows) {
+            for (int v = sub; v < vec_per_row; v += 16) {
+                const uint4 a = o[row * vec_per_row + v];
+                const uint4 bv = dO[row * vec_per_row + v];
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const float2 af = unpack2<BF16>(aw[x]);
+                    const float2 bf = unpack2<BF16>(bw[x]);
+                    acc = fmaf(af.x, bf.x, acc);
+                    acc = fmaf(af.y, bf.y, acc);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (sub == 0 && row < rows) Dvec[row] = acc;
+    }
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (long i = tid; i < acc_vec4; i += nthreads) dq_acc[i] = z;
+}
+
+// dQ = scale * dQacc in the element type; 8 elements per thread.
+template <bool BF16>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float4 *__restrict__ acc, uint4 *__restrict__ dq,
+                                                     long n8, float scale) {
+    const long nthreads = (long)gridDim.x * blockDim.x;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += nthreads) {
+        const float4 a = acc[2 * i];
+        const float4 c = acc[2 * i + 1];
+        uint4 out;
+        if constexpr (BF16) {
+            out = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                             pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
+        } else {
+            out = make_uint4(pack_f16x2(a.x * scale, a.y * scale), pack_f16x2(a.z * scale, a.w * scale),
+                             pack_f16x2(c.x * scale, c.y * scale), pack_f16x2(c.z * scale, c.w * scale));
+        }
+        dq[i] = out;
+    }
+}
+
+int elementwise_blocks() {
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms * 8;
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st) {
+    using L = BwdLayout<D>;
+    const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint64_t N = a.N;
+    const uint64_t pq = (uint64_t)a.B * a.Hq, pkv = (uint64_t)a.B * a.Hkv;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    if (!make_tmap_3d(&tq, a.q, dt, 2, D, N, pq, 64, kBQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_3d(&tdo, a.dO, dt, 2, D, N, pq, 64, kBQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_3d(&tk, a.k, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_3d(&tv, a.v, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_3d(&tdk, a.dk, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_3d(&tdv, a.dv, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+
+    const long rows = (long)a.B * a.Hq * a.N;
+    const int eb = elementwise_blocks();
+    bwd_pre_kernel<BF16><<<eb, 256, 0, st>>>(static_cast<const uint4 *>(a.o), static_cast<const uint4 *>(a.dO),
+                                             a.D, reinterpret_cast<float4 *>(a.dq_acc), rows, D,
+                                             rows * D / 4);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    e = cudaFuncSetAttribute(bwd_main_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    BwdParams p;
+    p.lse = a.lse;
+    p.Dvec = a.D;
+    p.dq_acc = a.dq_acc;
+    p.status = device_status_ptr();
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.N = a.N;
+    p.nkv = (a.N + kBKV - 1) / kBKV;
+    p.nq = (a.N + kBQ - 1) / kBQ;
+    p.causal = a.causal;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const long long grid = (long long)p.nkv * a.B * a.Hkv;
+    bwd_main_kernel<D, BF16><<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, tdo, tdk, tdv, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    bwd_dq_kernel<BF16><<<eb, 256, 0, st>>>(reinterpret_cast<const float4 *>(a.dq_acc),
+                                            static_cast<uint4 *>(a.dq), rows * D / 8, a.scale);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st) {
+    if (a.d == 128) return a.bf16 ? launch_bwd_t<128, true>(a, st) : launch_bwd_t<128, false>(a, st);
+    if (a.d == 64) return a.bf16 ? launch_bwd_t<64, true>(a, st) : launch_bwd_t<64, false>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fa
