@@ -17,7 +17,7 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA, FA
 FA_FP16, FA_BF16 = 0, 1
 
 EXPORTS = (
-    "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_hadamard_quant_fp8",
+    "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_noalloc", "fa_hadamard_quant_fp8",
     "fa_hadamard_quant_workspace_bytes", "fa_fwd_fp8", "fa_get_device_status",
     "fa_selftest_bounded_wait", "fa_status_string",
 )
@@ -45,6 +45,7 @@ def load():
         P, I, F, Z, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_long
         lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, Z, P]
+        lib.fa_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
         lib.fa_bwd_workspace_bytes.restype = Z
         lib.fa_hadamard_quant_fp8.argtypes = [P, P, P, P, L, I, P, Z, P]
@@ -55,7 +56,7 @@ def load():
         lib.fa_selftest_bounded_wait.argtypes = [I, P]
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_bwd", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
+        for name in ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
                      "fa_get_device_status", "fa_selftest_bounded_wait"):
             getattr(lib, name).restype = I
         _lib = lib
@@ -111,6 +112,16 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, workspac
     _check("fa_bwd", load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
                                    _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(causal), float(scale),
                                    _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, stream=None):
+    """fa_bwd using the library's built-in scratch buffer instead of a
+    caller workspace: for callers that cannot allocate device memory.  Calls
+    that may overlap on the GPU race on that buffer."""
+    B, Hq, Hkv, N, d = _dims(q, k)
+    _check("fa_bwd_noalloc", load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                                                   _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(causal),
+                                                   float(scale), _dtype_code(q), _stream(stream)))
 
 
 def fa_hadamard_quant_workspace_bytes(rows: int, d: int) -> int:

@@ -96,6 +96,38 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o,
                    size_t workspace_bytes, void *stream);
 
 /*
+ * Size of the scratch buffer built into the library for fa_bwd_noalloc:
+ * 64 MiB per device.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * fa_bwd without a workspace argument, for callers that cannot allocate
+ * device memory (code that may not call cudaMalloc, such as a plugin handed
+ * only tensor pointers by its host framework or a process whose memory pool
+ * is fixed up front).  The pages have no counterpart to this entry point; it
+ * exists only for such callers.
+ *   Arguments, layouts and results are exactly those of fa_bwd.  The
+ *   workspace is a buffer of FA_BWD_NOALLOC_SCRATCH_BYTES that lives inside
+ *   the library on every device that loads it, until the process exits.
+ *   Problems whose fa_bwd_workspace_bytes(B, Hq, N, d) exceeds that size are
+ *   refused with FA_ERR_WORKSPACE before anything touches the GPU (with
+ *   d = 128 this allows B * Hq * N up to about 130,000 rows).
+ *   The first call on a device (with that device current) looks up the
+ *   buffer's device address once; make that first call before any stream
+ *   capture.  The call allocates nothing.
+ *   All calls on a device share the one buffer: calls whose kernels may
+ *   overlap on the GPU (e.g. on unordered streams) race and give wrong
+ *   results.  Each call rewrites and re-zeroes what it uses, so nothing from
+ *   an earlier call carries over.
+ */
+fa_status_t fa_bwd_noalloc(const void *q, const void *k, const void *v,
+                           const void *o, const float *lse, const void *dO,
+                           void *dq, void *dk, void *dv, int B, int Hq,
+                           int Hkv, int N, int d, int causal, float scale,
+                           fa_dtype_t dtype, void *stream);
+
+/*
  * Bytes of workspace fa_hadamard_quant_fp8 needs (the fp32 amax cell).
  */
 size_t fa_hadamard_quant_workspace_bytes(long rows, int d);
