@@ -197,6 +197,7 @@ fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8, const flo
         if (!aligned16(p)) return FA_ERR_INVALID_ARG;
     fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
     if (s != FA_OK) return s;
+    if (d != 128) return FA_ERR_UNSUPPORTED;  // one 128-byte swizzle atom per e4m3 row
     fa::Fp8FwdArgs a{q8, k8, v8, q_descale, k_descale, v_descale, o_bf16, lse, B, Hq, Hkv, N, d,
                      causal ? 1 : 0, scale};
     return from_cuda(fa::launch_fwd_fp8(a, static_cast<cudaStream_t>(stream)));

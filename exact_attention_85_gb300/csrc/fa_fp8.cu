@@ -1,5 +1,544 @@
+// fa_fp8.cu -- FP8 (e4m3) path for sm_103a: random-sign Hadamard rotation
+// with per-tensor quantisation, and the FP8 forward.
+//
+// From the FlashAttention-3 summary page (vi.news.hada.io), "FP8" and
+// "incoherent processing": FP8 doubles tensor-core throughput; outliers in
+// Q and K inflate the quantisation error, which is reduced by multiplying Q
+// and K by a random orthogonal matrix -- a Hadamard transform with random
+// signs, O(d log d) per row -- which leaves Q K^T unchanged.
+//
+// Quantisation (two passes over the tensor, both memory bound):
+//   hq_amax_kernel   x' = (x o s) H_d / sqrt(d) per row (fast Walsh-Hadamard
+//                    butterflies in registers and warp shuffles), amax |x'|
+//   hq_quant_kernel  recomputes x', x8 = e4m3(x' * 448 / amax) (round to
+//                    nearest even, saturating), descale = amax / 448
+// With signs == NULL the rotation is skipped (plain per-tensor FP8).
+//
+// Forward (fwd_fp8_kernel): the structure of the bf16 forward (fa_fwd.cu)
+// with kind::f8f6f4 MMAs: Q, K, V e4m3 in 128-byte-swizzled shared memory
+// (one 128-byte row = 128 values, so d = 128 is one swizzle atom wide), P
+// quantised to e4m3 in tensor memory as the A operand of O += P V.  Scores are
+// descaled as S = scale * q_descale * k_descale * Q8 K8^T; O is multiplied by
+// v_descale in the epilogue.  P is lifted by 2^4 before quantisation so its
+// typical values sit in e4m3's normal range; the running max moves when a
+// tile's max exceeds it by more than 4 (log2 units), so P <= 2^8 < 448.  O is
+// normalised by the sum of the quantised P it was built from (the lift
+// cancels); L uses the sum of the unquantised P.
 #include "host_util.h"
+#include "ptx.cuh"
+
 namespace fa {
-cudaError_t launch_fwd_fp8(const Fp8FwdArgs &, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_hadamard_quant(const QuantArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+
+namespace {
+
+// ------------------------------------------------------------ e4m3 helpers
+
+// Two floats -> two e4m3 bytes (round to nearest even, saturating); `lo` in
+// bits 0-7.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
 }
+
+// Two e4m3 bytes (bits 0-15) -> two floats (exact).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v) {
+    uint32_t h2;
+    const uint16_t in = (uint16_t)v;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    float lo, hi;
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}\n"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+    return make_float2(lo, hi);
+}
+
+// --------------------------------------------- Hadamard + quantise kernels
+// Row layout: LPR = D / 8 lanes per row, 8 consecutive values per lane
+// (one 16-byte load), so a warp holds 32 / LPR rows.  Butterflies for
+// strides 1, 2, 4 run inside a lane; strides 8 .. D/2 pair lanes whose
+// in-row index differs in one bit.
+
+template <int D>
+__device__ __forceinline__ void hadamard_row(float (&x)[8], int sub) {
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if ((i & s) == 0) {
+                const float a = x[i], b = x[i + s];
+                x[i] = a + b;
+                x[i + s] = a - b;
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 1; m < D / 8; m <<= 1) {
+        const bool upper = (sub & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
+            x[i] = upper ? (other - x[i]) : (x[i] + other);
+        }
+    }
+    constexpr float inv_sqrt_d = D == 128 ? 0.08838834764831845f : 0.125f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] *= inv_sqrt_d;
+}
+
+template <int D>
+__device__ __forceinline__ void load_rotated(const uint4 *__restrict__ x, const float *__restrict__ signs, long row,
+                                             long rows, int sub, float (&v)[8]) {
+    if (row < rows) {
+        const uint4 u = x[row * (D / 8) + sub];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = unpack2<true>(w[i]);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+    if (signs) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] *= signs[sub * 8 + i];
+        hadamard_row<D>(v, sub);  // all lanes of the warp take part
+    }
+}
+
+__global__ void hq_zero_kernel(float *amax) { *amax = 0.0f; }
+
+template <int D>
+__global__ void __launch_bounds__(256) hq_amax_kernel(const uint4 *__restrict__ x, const float *__restrict__ signs,
+                                                      float *__restrict__ amax, long rows) {
+    constexpr int LPR = D / 8;
+    constexpr int RPW = 32 / LPR;
+    const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % LPR;
+    float m = 0.0f;
+    // warp-uniform trip count: the shuffles inside need every lane
+    for (long base = warp_id * RPW; base < rows; base += nwarps * RPW) {
+        float v[8];
+        load_rotated<D>(x, signs, base + lane / LPR, rows, sub, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    __shared__ float wmax[8];
+    if (lane == 0) wmax[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float bm = 0.0f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) bm = fmaxf(bm, wmax[i]);
+        // non-negative floats order like their bit patterns
+        atomicMax(reinterpret_cast<int *>(amax), __float_as_int(bm));
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) hq_quant_kernel(const uint4 *__restrict__ x, const float *__restrict__ signs,
+                                                       const float *__restrict__ amax, uint2 *__restrict__ x8,
+                                                       float *__restrict__ descale, long rows) {
+    constexpr int LPR = D / 8;
+    constexpr int RPW = 32 / LPR;
+    const float a = *amax;
+    const float inv = a > 0.0f ? 448.0f / a : 1.0f;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *descale = a > 0.0f ? a / 448.0f : 1.0f;
+    const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % LPR;
+    for (long base = warp_id * RPW; base < rows; base += nwarps * RPW) {
+        const long row = base + lane / LPR;
+        float v[8];
+        load_rotated<D>(x, signs, row, rows, sub, v);
+        if (row < rows) {
+            const uint32_t lo = cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+            const uint32_t hi = cvt_e4m3x2(v[4] * inv, v[5] * inv) | (cvt_e4m3x2(v[6] * inv, v[7] * inv) << 16);
+            x8[row * (D / 8) + sub] = make_uint2(lo, hi);
+        }
+    }
+}
+
+// ----------------------------------------------------------- FP8 forward
+
+constexpr int kBM = 128, kBN = 128, kD = 128;
+constexpr int kThreads = 224;
+constexpr float kRescaleThreshold = 4.0f;  // log2 units
+constexpr float kLift = 4.0f;              // P is quantised as 2^(s - m + kLift)
+
+struct Fp8Layout {
+    static constexpr int KS = 3, VS = 3;
+    static constexpr int TILE = kBM * kD;  // bytes (1 byte per value)
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + TILE;
+    static constexpr int OFF_V = OFF_K + KS * TILE;
+    static constexpr int OFF_O = OFF_V + VS * TILE;  // bf16 output staging, 2 boxes of 128 x 64
+    static constexpr int OFF_BAR = OFF_O + kBM * kD * 2;
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 + 2 + 1 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+
+struct Fp8Params {
+    float *lse;
+    const float *q_descale, *k_descale, *v_descale;
+    unsigned int *status;
+    int Hq, Hkv, N, nqt, causal;
+    float scale_log2;
+};
+
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // P buffers: 32 columns each
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const Fp8Params p) {
+    using L = Fp8Layout;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint64_t *q_full = bars;
+    uint64_t *k_full = q_full + 1;
+    uint64_t *k_empty = k_full + L::KS;
+    uint64_t *v_full = k_empty + L::KS;
+    uint64_t *v_empty = v_full + L::VS;
+    uint64_t *s_full = v_empty + L::VS;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *o_done = p_full + 2;
+    uint64_t *drain = o_done + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / p.nqt;
+    const int qt_lin = blockIdx.x - bh * p.nqt;
+    const int qt = p.causal ? (p.nqt - 1 - qt_lin) : qt_lin;
+    const int b = bh / p.Hq;
+    const int h = bh - b * p.Hq;
+    const int hk = h / (p.Hq / p.Hkv);
+    const int q0 = qt * kBM;
+    const int nkv_all = (p.N + kBN - 1) / kBN;
+    const int nkv = p.causal ? min(qt + 1, nkv_all) : nkv_all;
+    const int kv_plane = b * p.Hkv + hk;
+    const int q_plane = b * p.Hq + h;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < L::KS; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+        for (int s = 0; s < L::VS; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
+        for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&p_full[s], kBM); }
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ---------------------------------------------------- Q + K producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            mbar_arrive_expect_tx(q_full, L::TILE);
+            tma_load_3d(smem + L::OFF_Q, &tm_q, q_full, 0, q0, q_plane);
+            int j = 0;
+            for (; j < nkv; ++j) {
+                const int s = j % L::KS;
+                if (j >= L::KS && !mbar_wait(&k_empty[s], ((j / L::KS) + 1) & 1, abort_flag, p.status, 41)) break;
+                mbar_arrive_expect_tx(&k_full[s], L::TILE);
+                tma_load_3d(smem + L::OFF_K + s * L::TILE, &tm_k, &k_full[s], 0, j * kBN, kv_plane);
+            }
+            if (*abort_flag) {
+                for (int t = max(0, j - L::KS); t < j; ++t)
+                    mbar_wait_drain(&k_full[t % L::KS], (t / L::KS) & 1, 10000000ull);
+                mbar_wait_drain(q_full, 0, 10000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 6) {
+        // -------------------------------------------------------- V producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_v);
+            int j = 0;
+            for (; j < nkv; ++j) {
+                const int s = j % L::VS;
+                if (j >= L::VS && !mbar_wait(&v_empty[s], ((j / L::VS) + 1) & 1, abort_flag, p.status, 42)) break;
+                mbar_arrive_expect_tx(&v_full[s], L::TILE);
+                tma_load_3d(smem + L::OFF_V + s * L::TILE, &tm_v, &v_full[s], 0, j * kBN, kv_plane);
+            }
+            if (*abort_flag) {
+                for (int t = max(0, j - L::VS); t < j; ++t)
+                    mbar_wait_drain(&v_full[t % L::VS], (t / L::VS) & 1, 10000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            // kind::f8f6f4, e4m3 (format 0) for both operands, fp32 accumulate
+            constexpr uint32_t idesc_s = make_idesc(kBM, kBN, 0u, false, false);
+            constexpr uint32_t idesc_pv = make_idesc(kBM, kD, 0u, false, true);
+            const uint32_t q_addr = smem_u32(smem + L::OFF_Q);
+            bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 43);
+
+            auto issue_pv = [&](int t) -> bool {
+                const int pb = t & 1;
+                if (!mbar_wait(&p_full[pb], (t >> 1) & 1, abort_flag, p.status, 44)) return false;
+                const int vs = t % L::VS;
+                if (!mbar_wait(&v_full[vs], (t / L::VS) & 1, abort_flag, p.status, 45)) return false;
+                tc_fence_after();
+                const uint32_t v_addr = smem_u32(smem + L::OFF_V + vs * L::TILE);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 32; ++kk) {
+                    // B = V: head dim contiguous (MN-major), 32 keys = 32 rows of 128 B
+                    const uint64_t bdesc = make_sdesc_sw128(v_addr + kk * 32 * 128, 0, 1024);
+                    mma_f8_ts(tmem + kColO, tmem + kColP + pb * 32 + kk * 8, bdesc, idesc_pv,
+                              (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(o_done);
+                mma_commit(&v_empty[vs]);
+                return true;
+            };
+
+            for (int j = 0; ok && j < nkv; ++j) {
+                const int ks = j % L::KS;
+                if (!mbar_wait(&k_full[ks], (j / L::KS) & 1, abort_flag, p.status, 46)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t k_addr = smem_u32(smem + L::OFF_K + ks * L::TILE);
+                const uint32_t s_col = tmem + kColS + (j & 1) * kBN;
+#pragma unroll
+                for (int kk = 0; kk < kD / 32; ++kk) {
+                    const uint64_t adesc = make_sdesc_sw128(q_addr + kk * 32, 16, 1024);
+                    const uint64_t bdesc = make_sdesc_sw128(k_addr + kk * 32, 16, 1024);
+                    mma_f8_ss(s_col, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&s_full[j & 1]);
+                mma_commit(&k_empty[ks]);
+                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+            }
+            if (ok && nkv > 0) issue_pv(nkv - 1);
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ softmax + epilogue
+        const int row = threadIdx.x;  // 0..127 == TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const float sl2 = p.scale_log2 * (*p.q_descale) * (*p.k_descale);
+        float m_ref = -INFINITY;
+        float l_sum = 0.0f;    // sum of the quantised P (lifted): normalises O
+        float l_exact = 0.0f;  // sum of the unquantised P (lifted): gives L
+        bool ok = true;
+        uint32_t s[128];
+
+        for (int j = 0; j < nkv; ++j) {
+            const int sb = j & 1;
+            const bool got_s = mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.status, 47);
+            if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t s_addr = lane_base + kColS + sb * kBN;
+            tmem_ld_x32(s_addr + 0, s + 0);
+            tmem_ld_x32(s_addr + 32, s + 32);
+            tmem_ld_x32(s_addr + 64, s + 64);
+            tmem_ld_x32(s_addr + 96, s + 96);
+            tmem_ld_wait_x32(s + 0);
+            tmem_ld_wait_x32(s + 32);
+            tmem_ld_wait_x32(s + 64);
+            tmem_ld_wait_x32(s + 96);
+
+            const int kv0 = j * kBN;
+            const bool need_mask = (kv0 + kBN > p.N) || (p.causal && kv0 + kBN - 1 > q0);
+            if (need_mask) {
+                const int lim = p.causal ? min(p.N, q0 + row + 1) : p.N;
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (kv0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
+            }
+            float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
+            float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
+#pragma unroll
+            for (int c = 4; c < 128; c += 4) {
+                mx0 = fmaxf(mx0, __uint_as_float(s[c]));
+                mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
+                mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
+                mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
+            }
+            const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            float alpha = 1.0f;
+            bool rescale = false;
+            if (mx > m_ref + kRescaleThreshold) {
+                alpha = ex2_approx(m_ref - mx);
+                l_sum *= alpha;
+                l_exact *= alpha;
+                m_ref = mx;
+                rescale = true;
+            }
+            const float bias = kLift - m_ref;
+            float l0 = 0.f, l1 = 0.f, e0 = 0.f, e1 = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+                const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, bias));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, bias));
+                const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), sl2, bias));
+                const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), sl2, bias));
+                const uint32_t w01 = cvt_e4m3x2(p0, p1);
+                const uint32_t w23 = cvt_e4m3x2(p2, p3);
+                pk[c / 4] = w01 | (w23 << 16);
+                const float2 r01 = e4m3x2_to_float2(w01);
+                const float2 r23 = e4m3x2_to_float2(w23);
+                l0 += r01.x + r01.y;
+                l1 += r23.x + r23.y;
+                e0 += p0 + p1;
+                e1 += p2 + p3;
+            }
+            l_sum += l0 + l1;
+            l_exact += e0 + e1;
+            __syncwarp();
+            tmem_st_x32(lane_base + kColP + sb * 32, pk);
+
+            if (j >= 1) {
+                const bool got_o = mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status, 48);
+                if (!__all_sync(0xffffffffu, got_o)) { ok = false; break; }
+                if (__any_sync(0xffffffffu, rescale)) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < kD; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld_x32(lane_base + kColO + c0, o);
+                        tmem_ld_wait_x32(o);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st_x32(lane_base + kColO + c0, o);
+                    }
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&p_full[sb]);
+        }
+
+        if (ok && nkv > 0) ok = mbar_wait(o_done, (nkv - 1) & 1, abort_flag, p.status, 49);
+        __syncwarp();
+        ok = named_bar_and(1, kBM, ok);
+        if (ok) {
+            tc_fence_after();
+            // O = v_descale * O~ / l, bf16, staged in the 128-byte-swizzled
+            // layout of two 64-column output boxes
+            const float f = (*p.v_descale) / l_sum;
+            uint8_t *stage = smem + L::OFF_O;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld_x32(lane_base + kColO + c0, o);
+                tmem_ld_wait_x32(o);
+                uint32_t w[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * f, __uint_as_float(o[2 * c + 1]) * f);
+                uint8_t *rowp = stage + (c0 >> 6) * (kBM * 128) + row * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = ((c0 & 63) >> 3) + q;
+                    *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, kBM);
+            if (row == 0) {
+                for (int bx = 0; bx < 2; ++bx) tma_store_3d(&tm_o, stage + bx * (kBM * 128), bx * 64, q0, q_plane);
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+            if (q0 + row < p.N)
+                p.lse[(size_t)q_plane * p.N + q0 + row] =
+                    (m_ref + log2f(l_exact) - kLift) * 0.69314718055994530942f;
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+int stream_blocks() {
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms * 8;
+}
+
+template <int D>
+cudaError_t launch_hq_t(const QuantArgs &a, cudaStream_t st) {
+    const int nb = stream_blocks();
+    hq_zero_kernel<<<1, 1, 0, st>>>(a.amax);
+    hq_amax_kernel<D><<<nb, 256, 0, st>>>(static_cast<const uint4 *>(a.x), a.signs, a.amax, a.rows);
+    hq_quant_kernel<D><<<nb, 256, 0, st>>>(static_cast<const uint4 *>(a.x), a.signs, a.amax,
+                                           static_cast<uint2 *>(a.x8), a.descale, a.rows);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_hadamard_quant(const QuantArgs &a, cudaStream_t st) {
+    if (a.d == 128) return launch_hq_t<128>(a, st);
+    if (a.d == 64) return launch_hq_t<64>(a, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_fp8(const Fp8FwdArgs &a, cudaStream_t st) {
+    if (a.d != kD) return cudaErrorInvalidValue;
+    using L = Fp8Layout;
+    CUtensorMap tq, tk, tv, to;
+    const uint64_t N = a.N;
+    if (!make_tmap_3d(&tq, a.q8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kD, N, (uint64_t)a.B * a.Hq, 128, kBM,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_3d(&tk, a.k8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kD, N, (uint64_t)a.B * a.Hkv, 128, kBN,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_3d(&tv, a.v8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, kD, N, (uint64_t)a.B * a.Hkv, 128, kBN,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_3d(&to, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, N, (uint64_t)a.B * a.Hq, 64, kBM,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(fwd_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    Fp8Params p;
+    p.lse = a.lse;
+    p.q_descale = a.q_descale;
+    p.k_descale = a.k_descale;
+    p.v_descale = a.v_descale;
+    p.status = device_status_ptr();
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.N = a.N;
+    p.nqt = (a.N + kBM - 1) / kBM;
+    p.causal = a.causal;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const long long grid = (long long)p.nqt * a.B * a.Hq;
+    fwd_fp8_kernel<<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, to, p);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -159,6 +159,12 @@ fa_status_t fa_hadamard_quant_fp8(const void *x_bf16, const float *signs,
  * [FA3] "FP8" (tensor-core throughput doubles at 8 bits) and the FP8 forward
  * figures of that page.  Q and K may have been rotated by the same random-sign
  * Hadamard matrix, which leaves Q K^T unchanged.
+ *   q8 [B][Hq][N][d], k8, v8 [B][Hkv][N][d]: e4m3 bytes (in)
+ *   q/k/v_descale: one fp32 device scalar each (in), as written by
+ *   fa_hadamard_quant_fp8
+ *   o_bf16 [B][Hq][N][d] bf16 (out); lse [B][Hq][N] fp32 (out)
+ * d must be 128 (FA_ERR_UNSUPPORTED otherwise).  P is quantised to e4m3
+ * before the P.V product, so O carries FP8 rounding of both operands.
  */
 fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8,
                        const float *q_descale, const float *k_descale,
