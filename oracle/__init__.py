@@ -179,17 +179,10 @@ def e4m3_round(x):
     return out
 
 
-def fp8_reference(q, k, v, signs, causal: bool, scale: float):
-    """Diagnostic model of the FP8 path's input quantisation.
-
-    Q and K are rotated by the random-sign Hadamard (if ``signs`` is not
-    None), then Q, K and V are each quantised per tensor to e4m3 with
-    sigma = amax / 448, dequantised, and fed to the exact fp64 attention.
-    The rotation is orthogonal, so without quantisation this returns exactly
-    ``attention_fwd(q, k, v)``.  It separates the error of input
-    quantisation from that of a kernel; the error level itself is parity
-    unpinned by the pages, which report only a 2.6x ratio.
-    """
+def fp8_dequantized(q, k, v, signs):
+    """Q, K, V as the FP8 path sees them: Q and K rotated by the random-sign
+    Hadamard (if ``signs`` is not None), each tensor quantised per tensor to
+    e4m3 with sigma = amax / 448 and dequantised (fp64)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     if signs is not None:
         q = hadamard(q, signs)
@@ -201,4 +194,18 @@ def fp8_reference(q, k, v, signs, causal: bool, scale: float):
             return x
         return e4m3_round(x / sigma) * sigma
 
-    return attention_fwd(qdq(q), qdq(k), qdq(v), causal, scale)
+    return qdq(q), qdq(k), qdq(v)
+
+
+def fp8_reference(q, k, v, signs, causal: bool, scale: float):
+    """Diagnostic model of the FP8 path's input quantisation.
+
+    Q and K are rotated by the random-sign Hadamard (if ``signs`` is not
+    None), then Q, K and V are each quantised per tensor to e4m3 with
+    sigma = amax / 448, dequantised, and fed to the exact fp64 attention.
+    The rotation is orthogonal, so without quantisation this returns exactly
+    ``attention_fwd(q, k, v)``.  It separates the error of input
+    quantisation from that of a kernel; the error level itself is parity
+    unpinned by the pages, which report only a 2.6x ratio.
+    """
+    return attention_fwd(*fp8_dequantized(q, k, v, signs), causal, scale)

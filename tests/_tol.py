@@ -5,8 +5,8 @@ at |O_ref|, element-wise.  The 4e-3 bound is the stated O tolerance; the
 half-ulp term is the rounding of the stored output itself, which alone can
 exceed 4e-3 for bf16 values of magnitude >= 1 (ulp 2^-7 on [1, 2)).
 LSE: max-abs <= 1e-3.  Gradients: relative Frobenius error <= 1e-2 per tensor.
-FP8 O: relative RMS error <= 0.03, and no worse than the same kernel without
-the Hadamard rotation.
+FP8 O: RMS error relative to the RMS of V <= 0.03, and no worse than the
+same kernel without the Hadamard rotation.
 """
 import numpy as np
 import torch
