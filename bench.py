@@ -40,6 +40,7 @@ def _args():
     ap.add_argument("--workload", default=None, help="workload name (default: the headline shape)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 leg (outlier workload)")
     return ap.parse_args()
 
 
@@ -252,6 +253,8 @@ def run_ours(a):
         "clocks": clk.summary(),
     }
 
+    if not a.no_fp8 and a.workload is None:
+        result["fp8_leg"] = _fp8_leg(a, dev, stream, peaks)
     if not a.no_e2e:
         result["e2e"] = _e2e(a, w, host, dev, stream, has_bwd, ws)
     if rank == 0 and ws == 1 and not a.no_cpu:
@@ -260,6 +263,67 @@ def run_ours(a):
         print(json.dumps(result), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def _fp8_leg(a, dev, stream, peaks):
+    """The FP8 rows of the path on their own workload (B4 H16 N8192 d128,
+    non-causal, 0.1% outliers): random-sign Hadamard + e4m3 quantisation of
+    Q and K, plain quantisation of V, then the FP8 forward.  Reported beside
+    the bf16 step, not part of it."""
+    import torch
+
+    from exact_attention_85_gb300 import _lib
+    from exact_attention_85_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS["fp8_b4_h16_n8k_outliers"]
+    host = make_inputs(w, with_grad=False)
+    q, k, v = (host[n].to(dev).contiguous() for n in ("q", "k", "v"))
+    signs = host["signs"].to(dev)
+    B, Hq, N, d = q.shape
+    q8, k8, v8 = (torch.empty(t.shape, dtype=torch.uint8, device=dev) for t in (q, k, v))
+    ds = torch.empty(3, dtype=torch.float32, device=dev)
+    ws = torch.empty(3 * 256, dtype=torch.uint8, device=dev)
+    o = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def quant():
+        _lib.fa_hadamard_quant_fp8(q, signs, q8, ds[0:1], ws[0:256], stream)
+        _lib.fa_hadamard_quant_fp8(k, signs, k8, ds[1:2], ws[256:512], stream)
+        _lib.fa_hadamard_quant_fp8(v, None, v8, ds[2:3], ws[512:768], stream)
+
+    def fwd():
+        _lib.fa_fwd_fp8(q8, k8, v8, ds[0:1], ds[1:2], ds[2:3], o, lse, w.causal, w.scale, stream)
+
+    for _ in range(max(3, a.warmup)):
+        quant()
+        fwd()
+        flush.zero_()
+    torch.cuda.synchronize()
+    steps = max(3, min(a.steps, 10))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        quant()
+        ev[i][1].record(stream)
+        fwd()
+        ev[i][2].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if _lib.fa_get_device_status(stream) != _lib.FA_OK:
+        raise RuntimeError("a bounded device wait ran out during the FP8 leg")
+    q_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    f_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    tflops = w.fwd_flops() / (f_ms * 1e-3) / 1e12
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    q_bytes = 3 * q.numel() * (2 + 1)  # algorithmic: read bf16 once, write e4m3 once
+    return {"workload": w.name, "fwd_ms": round(f_ms, 4), "fwd_tflops": round(tflops, 1),
+            "fwd_frac_of_fp8_peak": round(tflops / fp8_peak, 4),
+            "fp8_peak": fp8_peak, "fp8_peak_source": f"2 x {peaks['source']} bf16 burst (nominal FP8/BF16 ratio)",
+            "quant_ms_3_tensors": round(q_ms, 4),
+            "quant_gbs_algorithmic": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
+            "quant_frac_of_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "launches_per_step": 3 * 3 + 1}
 
 
 def _e2e(a, w, host, dev, stream, has_bwd, ws):

@@ -202,8 +202,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_sdp = make_idesc(kBKV, kBQ, fmt, false, false);  // K-major both
             constexpr uint32_t idesc_acc = make_idesc(kBKV, D, fmt, false, true);     // A tmem, B MN-major
             constexpr uint32_t idesc_dq = make_idesc(kBKV, kBQ, fmt, true, true);     // A, B MN-major
-            const uint32_t k_addr = smem_u32(smem + L::OFF_K);
-            const uint32_t v_addr = smem_u32(smem + L::OFF_V);
+            // one descriptor per operand tile; steps are derived by sdesc_advance
+            const uint64_t k_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);  // K-major
+            const uint64_t v_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_V), 16, 1024);
+            // K^T as the MN-major A of dQ^T; for d = 64 the second 64-row half of
+            // A repeats the first (LBO 0) and those rows are never read out
+            const uint64_t kt_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_K), D == 128 ? L::BOX_KV : 0, 1024);
+            const uint64_t qk_desc0 = make_sdesc_sw128(smem_u32(q_stage(0)), 16, 1024);          // K-major
+            const uint64_t dok_desc0 = make_sdesc_sw128(smem_u32(do_stage(0)), 16, 1024);
+            const uint64_t qm_desc0 = make_sdesc_sw128(smem_u32(q_stage(0)), L::BOX_Q, 1024);    // MN-major
+            const uint64_t dom_desc0 = make_sdesc_sw128(smem_u32(do_stage(0)), L::BOX_Q, 1024);
+            const uint64_t ds_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_DS), 0, 1024);
+            constexpr uint32_t kStage = 2 * L::TILE_Q;  // bytes between Q/dO stages
             bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 22);
 
             // S^T = K_j Q_t^T and dP^T = V_j dO_t^T into tensor-memory buffer t % 2
@@ -212,21 +222,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = t % QS;
                 if (!mbar_wait(&qd_full[st], (t / QS) & 1, abort_flag, p.status, 23)) return false;
                 tc_fence_after();
-                const uint32_t q_addr = smem_u32(q_stage(st));
-                const uint32_t do_addr = smem_u32(do_stage(st));
+                const uint64_t q_desc = sdesc_advance(qk_desc0, st * kStage);
+                const uint64_t do_desc = sdesc_advance(dok_desc0, st * kStage);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
                     const uint32_t oq = (kk >> 2) * L::BOX_Q + (kk & 3) * 32;
-                    mma_f16_ss(tmem + bb * 128, make_sdesc_sw128(k_addr + okv, 16, 1024),
-                               make_sdesc_sw128(q_addr + oq, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
+                    mma_f16_ss(tmem + bb * 128, sdesc_advance(k_desc, okv), sdesc_advance(q_desc, oq), idesc_sdp,
+                               kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
                     const uint32_t oq = (kk >> 2) * L::BOX_Q + (kk & 3) * 32;
-                    mma_f16_ss(tmem + bb * 128 + 64, make_sdesc_sw128(v_addr + okv, 16, 1024),
-                               make_sdesc_sw128(do_addr + oq, 16, 1024), idesc_sdp, kk > 0 ? 1u : 0u);
+                    mma_f16_ss(tmem + bb * 128 + 64, sdesc_advance(v_desc, okv), sdesc_advance(do_desc, oq),
+                               idesc_sdp, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&sdp_full[bb]);
                 return true;
@@ -239,29 +249,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int st = it % QS;
                 if (!mbar_wait(&ds_ready[bb], (it >> 1) & 1, abort_flag, p.status, 24)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t ds_addr = smem_u32(smem + L::OFF_DS + bb * L::DS_BYTES);
+                const uint64_t ds_desc = sdesc_advance(ds_desc0, bb * L::DS_BYTES);
                 // dQ_i^T = K_j^T dS_i^T: A = K^T (head dim contiguous: MN-major), B = dS^T
-                // rows of keys in shared memory (MN-major).  For d = 64 the second
-                // 64-row half of A repeats the first (LBO 0); those rows are unused.
+                // rows of keys in shared memory (MN-major); 16 keys = 2048 bytes per step
 #pragma unroll
                 for (int kk = 0; kk < kBKV / 16; ++kk)
-                    mma_f16_ss(tmem + bb * 128 + 64,
-                               make_sdesc_sw128(k_addr + kk * 2048, D == 128 ? L::BOX_KV : 0, 1024),
-                               make_sdesc_sw128(ds_addr + kk * 2048, 0, 1024), idesc_dq, kk > 0 ? 1u : 0u);
+                    mma_f16_ss(tmem + bb * 128 + 64, sdesc_advance(kt_desc, kk * 2048),
+                               sdesc_advance(ds_desc, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
                 mma_commit(&dq_full[bb]);
-                const uint32_t q_addr = smem_u32(q_stage(st));
-                const uint32_t do_addr = smem_u32(do_stage(st));
+                const uint64_t qm_desc = sdesc_advance(qm_desc0, st * kStage);
+                const uint64_t dom_desc = sdesc_advance(dom_desc0, st * kStage);
+                const uint32_t acc_first = it > 0 ? 1u : 0u;
                 // dV_j += P^T dO_i and dK_j += dS^T Q_i (A from tensor memory)
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDV, tmem + bb * 128 + kk * 8,
-                               make_sdesc_sw128(do_addr + kk * 2048, L::BOX_Q, 1024), idesc_acc,
-                               (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_f16_ts(tmem + kColDV, tmem + bb * 128 + kk * 8, sdesc_advance(dom_desc, kk * 2048),
+                               idesc_acc, kk > 0 ? 1u : acc_first);
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDK, tmem + bb * 128 + 32 + kk * 8,
-                               make_sdesc_sw128(q_addr + kk * 2048, L::BOX_Q, 1024), idesc_acc,
-                               (it > 0 || kk > 0) ? 1u : 0u);
+                    mma_f16_ts(tmem + kColDK, tmem + bb * 128 + 32 + kk * 8, sdesc_advance(qm_desc, kk * 2048),
+                               idesc_acc, kk > 0 ? 1u : acc_first);
                 mma_commit(&qd_empty[st]);
                 if (it + 2 < n_it) {
                     // buffer bb is reused once dQ_i^T has been read out of it

@@ -295,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // kind::f8f6f4, e4m3 (format 0) for both operands, fp32 accumulate
             constexpr uint32_t idesc_s = make_idesc(kBM, kBN, 0u, false, false);
             constexpr uint32_t idesc_pv = make_idesc(kBM, kD, 0u, false, true);
-            const uint32_t q_addr = smem_u32(smem + L::OFF_Q);
+            const uint64_t q_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_Q), 16, 1024);
+            const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);
+            const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_V), 0, 1024);
             bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 43);
 
             auto issue_pv = [&](int t) -> bool {
@@ -304,14 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int vs = t % L::VS;
                 if (!mbar_wait(&v_full[vs], (t / L::VS) & 1, abort_flag, p.status, 45)) return false;
                 tc_fence_after();
-                const uint32_t v_addr = smem_u32(smem + L::OFF_V + vs * L::TILE);
+                const uint64_t v_desc = sdesc_advance(v_desc0, vs * L::TILE);
+                const uint32_t p_col = tmem + kColP + pb * 32;
+                // B = V: head dim contiguous (MN-major), 32 keys = 32 rows of 128 B
+                mma_f8_ts(tmem + kColO, p_col, v_desc, idesc_pv, t > 0 ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 32; ++kk) {
-                    // B = V: head dim contiguous (MN-major), 32 keys = 32 rows of 128 B
-                    const uint64_t bdesc = make_sdesc_sw128(v_addr + kk * 32 * 128, 0, 1024);
-                    mma_f8_ts(tmem + kColO, tmem + kColP + pb * 32 + kk * 8, bdesc, idesc_pv,
-                              (t > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < kBN / 32; ++kk)
+                    mma_f8_ts(tmem + kColO, p_col + kk * 8, sdesc_advance(v_desc, kk * 32 * 128), idesc_pv, 1u);
                 mma_commit(o_done);
                 mma_commit(&v_empty[vs]);
                 return true;
@@ -321,14 +322,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ks = j % L::KS;
                 if (!mbar_wait(&k_full[ks], (j / L::KS) & 1, abort_flag, p.status, 46)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t k_addr = smem_u32(smem + L::OFF_K + ks * L::TILE);
+                const uint64_t k_desc = sdesc_advance(k_desc0, ks * L::TILE);
                 const uint32_t s_col = tmem + kColS + (j & 1) * kBN;
 #pragma unroll
-                for (int kk = 0; kk < kD / 32; ++kk) {
-                    const uint64_t adesc = make_sdesc_sw128(q_addr + kk * 32, 16, 1024);
-                    const uint64_t bdesc = make_sdesc_sw128(k_addr + kk * 32, 16, 1024);
-                    mma_f8_ss(s_col, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kD / 32; ++kk)
+                    mma_f8_ss(s_col, sdesc_advance(q_desc, kk * 32), sdesc_advance(k_desc, kk * 32), idesc_s,
+                              kk > 0 ? 1u : 0u);
                 mma_commit(&s_full[j & 1]);
                 mma_commit(&k_empty[ks]);
                 if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }

@@ -177,7 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t fmt = BF16 ? 1u : 0u;
             constexpr uint32_t idesc_s = make_idesc(kBM, kBN, fmt, false, false);
             constexpr uint32_t idesc_pv = make_idesc(kBM, D, fmt, false, true);
-            const uint32_t q_addr = smem_u32(smem + L::OFF_Q);
+            // one descriptor per operand tile; steps are derived by sdesc_advance
+            const uint64_t q_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_Q), 16, 1024);
+            const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);
+            const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_V), kBN * 128, 1024);
             bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 3);
 
             auto issue_pv = [&](int t) -> bool {
@@ -186,14 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int vs = t % L::VS;
                 if (!mbar_wait(&v_full[vs], (t / L::VS) & 1, abort_flag, p.status, 5)) return false;
                 tc_fence_after();
-                const uint32_t v_addr = smem_u32(smem + L::OFF_V + vs * L::TILE_KV);
+                const uint64_t v_desc = sdesc_advance(v_desc0, vs * L::TILE_KV);
+                const uint32_t p_col = tmem + kColP + pb * 64;
+                // B = V (N = d contiguous: MN-major); 16 keys = 16 rows of 128 B
+                mma_f16_ts(tmem + kColO, p_col, v_desc, idesc_pv, t > 0 ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // B = V (N = d contiguous: MN-major); 16 keys = 16 rows of 128 B
-                    const uint64_t bdesc = make_sdesc_sw128(v_addr + kk * 16 * 128, kBN * 128, 1024);
-                    mma_f16_ts(tmem + kColO, tmem + kColP + pb * 64 + kk * 8, bdesc, idesc_pv,
-                               (t > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < kBN / 16; ++kk)
+                    mma_f16_ts(tmem + kColO, p_col + kk * 8, sdesc_advance(v_desc, kk * 16 * 128), idesc_pv, 1u);
                 mma_commit(o_done);
                 mma_commit(&v_empty[vs]);
                 return true;
@@ -203,14 +205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ks = j % L::KS;
                 if (!mbar_wait(&k_full[ks], (j / L::KS) & 1, abort_flag, p.status, 6)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t k_addr = smem_u32(smem + L::OFF_K + ks * L::TILE_KV);
+                const uint64_t k_desc = sdesc_advance(k_desc0, ks * L::TILE_KV);
                 const uint32_t s_col = tmem + kColS + (j & 1) * kBN;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-                    const uint64_t adesc = make_sdesc_sw128(q_addr + off, 16, 1024);
-                    const uint64_t bdesc = make_sdesc_sw128(k_addr + off, 16, 1024);
-                    mma_f16_ss(s_col, adesc, bdesc, idesc_s, kk > 0 ? 1u : 0u);
+                    mma_f16_ss(s_col, sdesc_advance(q_desc, off), sdesc_advance(k_desc, off), idesc_s,
+                               kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&s_full[j & 1]);
                 mma_commit(&k_empty[ks]);

@@ -252,6 +252,15 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
     return desc;
 }
 
+// Advances a shared-memory descriptor by `bytes` (a multiple of 16).  The
+// start address is the low field in 16-byte units, so a plain add moves it;
+// every operand here lies inside the 256 KB shared window, so the field never
+// carries into the next one.  Lets MMA issue loops build one descriptor per
+// tile and derive the per-step ones with a single add.
+__host__ __device__ constexpr uint64_t sdesc_advance(uint64_t d, uint32_t bytes) {
+    return d + (uint64_t)(bytes >> 4);
+}
+
 // ---------------------------------------------------- TMEM loads and stores
 // 32x32b shape: thread t of the warp accesses TMEM lane (lane field + t);
 // .xN moves N consecutive 32-bit columns.
