@@ -17,19 +17,21 @@
 //   bwd_dq_kernel    dQ = scale * dQacc, converted to the element type
 //
 // Main kernel, one CTA per (128-key tile, key/value head, batch); Q tiles of
-// 64 rows.  Tensor memory (512 columns, fp32, lane = key row unless noted):
-//   buffer b (b = 0, 1; base 128 b):
-//     [0, 64)   S^T = K_j Q_i^T       -> then [0, 32) P^T, [32, 64) dS^T (16-bit pairs)
-//     [64, 128) dP^T = V_j dO_i^T     -> then dQ_i^T = K_j^T dS_i^T (lane = head-dim index)
+// 128 rows, so every MMA is 128 x 128 (full tensor-core rate; at 64 columns the
+// shared-memory operand traffic caps the rate near two thirds).  Tensor
+// memory (512 columns, fp32, lane = key row unless noted):
+//   [0, 128)   S^T = K_j Q_i^T    -> then, per 32-query chunk m, P^T in
+//              [32 m, 32 m + 16) and dS^T in [32 m + 16, 32 m + 32) (16-bit pairs)
+//   [128, 256) dP^T = V_j dO_i^T  -> then dQ_i^T = K_j^T dS_i^T (lane = head-dim index)
 //   [256, 256 + d) dV_j,  [384, 384 + d) dK_j  (accumulated over all Q tiles)
 // P^T and dS^T stay in tensor memory as the A operands of dV += P^T dO and
 // dK += dS^T Q; dS^T is also written to shared memory as the B operand of
-// dQ^T = K^T dS^T.  dQ^T is read out by four warps and added into dQacc with
-// fp32 atomic reductions (one 128-byte line per warp and query row).
-// Warps: 0-3 and 10-13 softmax (P, dS; warps 0-3 then store dV), 4 TMA
-// producer, 5 MMA issuer + TMEM owner, 6-9 dQ read-out (then store dK).
-// Q / dO tiles stream through a 3-deep ring so their loads are issued two
-// tiles ahead of use.
+// dQ^T = K^T dS^T.  Per Q tile: MMA S^T, dP^T -> softmax warps -> MMA dQ^T,
+// dV, dK -> the same warps read dQ^T out (which frees the columns for the next
+// S^T, dP^T) and add it into dQacc with fp32 atomic reductions (one 128-byte
+// line per warp and query row) while the tensor cores run on.
+// Warps: 0-7 softmax + dQ read-out (then 0-3 store dV, 4-7 store dK),
+// 8 TMA producer (Q / dO through a 2-deep ring), 9 MMA issuer + TMEM owner.
 #include "host_util.h"
 #include "ptx.cuh"
 
@@ -37,10 +39,10 @@ namespace fa {
 
 namespace {
 
-constexpr int kBQ = 64;        // query rows per Q tile
+constexpr int kBQ = 128;       // query rows per Q tile
 constexpr int kBKV = 128;      // key rows per CTA (TMEM lanes)
-constexpr int kThreads = 448;  // 14 warps
-constexpr int kSoftmaxThreads = 256;
+constexpr int kThreads = 320;  // 10 warps
+constexpr int kWorkThreads = 256;  // warps 0-7: softmax, dQ read-out, epilogue
 
 template <int D>
 struct BwdLayout {
@@ -49,22 +51,23 @@ struct BwdLayout {
     static constexpr int TILE_Q = kBQ * D * 2;    // Q or dO tile
     static constexpr int BOX_KV = kBKV * 128;     // one 64-column box of a K/V tile
     static constexpr int BOX_Q = kBQ * 128;       // one 64-column box of a Q/dO tile
-    static constexpr int QS = 3;                  // Q/dO ring depth
-    static constexpr int DS_BYTES = kBKV * kBQ * 2;
+    static constexpr int QS = 2;                  // Q/dO ring depth
+    static constexpr int DS_BYTES = kBKV * kBQ * 2;  // dS^T: two 64-query boxes
+    static constexpr int DS_BOX = kBKV * 128;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + TILE_KV;
     static constexpr int OFF_QD = OFF_V + TILE_KV;  // stage s: Q at +2s*TILE_Q, dO at +(2s+1)*TILE_Q
     static constexpr int OFF_DS = OFF_QD + QS * 2 * TILE_Q;
-    static constexpr int OFF_LD = OFF_DS + 2 * DS_BYTES;  // stage s: L2[64], D[64]
+    static constexpr int OFF_LD = OFF_DS + DS_BYTES;  // stage s: L2[128], D[128]
     static constexpr int OFF_BAR = OFF_LD + QS * 2 * kBQ * 4;
-    // kv_full, qd_full[QS], qd_empty[QS], sdp_full[2], ds_ready[2], dq_full[2],
-    // dq_free[2], acc_done, drain
-    static constexpr int NBAR = 1 + 2 * QS + 2 * 4 + 2;
+    // kv_full, qd_full[QS], qd_empty[QS], sdp_full, ds_ready, dq_full, dq_free,
+    // acc_done, drain
+    static constexpr int NBAR = 1 + 2 * QS + 4 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
-    static constexpr int ALLOC = BYTES + 1024;
-    // the dV / dK epilogue stages each 128 x d output tile in one Q/dO stage
-    static_assert(2 * TILE_Q >= TILE_KV, "an output tile must fit in one Q/dO stage");
+    static constexpr int SLACK = 512;  // room to align the dynamic shared base up to 1024
+    static constexpr int ALLOC = BYTES + SLACK;
+    static_assert(TILE_Q >= TILE_KV, "an output tile must fit in one Q (or dO) buffer");
 };
 
 struct BwdParams {
@@ -77,7 +80,8 @@ struct BwdParams {
     float scale, scale_log2;
 };
 
-constexpr uint32_t kColDV = 256, kColDK = 384;
+// tensor-memory columns
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 128, kColDV = 256, kColDK = 384;
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -88,16 +92,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = BwdLayout<D>;
     constexpr int QS = L::QS;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    if (pad > (uint32_t)L::SLACK) {  // uniform across the CTA; nothing started yet
+        if (threadIdx.x == 0) record_timeout(p.status, 0x7FFF);
+        return;
+    }
+    uint8_t *smem = smem_raw + pad;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *kv_full = bars;
     uint64_t *qd_full = bars + 1;
     uint64_t *qd_empty = qd_full + QS;
     uint64_t *sdp_full = qd_empty + QS;
-    uint64_t *ds_ready = sdp_full + 2;
-    uint64_t *dq_full = ds_ready + 2;
-    uint64_t *dq_free = dq_full + 2;
-    uint64_t *acc_done = dq_free + 2;
+    uint64_t *ds_ready = sdp_full + 1;
+    uint64_t *dq_full = ds_ready + 1;
+    uint64_t *dq_free = dq_full + 1;
+    uint64_t *acc_done = dq_free + 1;
     uint64_t *drain = acc_done + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
@@ -112,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = bg - b * p.Hkv;
     const int G = p.Hq / p.Hkv;
     const int kv0 = jt * kBKV;
-    const int i_start = p.causal ? 2 * jt : 0;  // first Q tile with a row >= kv0
+    const int i_start = p.causal ? jt : 0;  // first Q tile with a row >= kv0 (equal tile sizes)
     const int n_i = p.nq - i_start;
     const int n_it = G * n_i;
 
@@ -124,18 +133,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&qd_full[s], 33);
             mbar_init(&qd_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&sdp_full[s], 1);
-            mbar_init(&ds_ready[s], kSoftmaxThreads);
-            mbar_init(&dq_full[s], 1);
-            mbar_init(&dq_free[s], 128);
-        }
+        mbar_init(sdp_full, 1);
+        mbar_init(ds_ready, kWorkThreads);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_free, kWorkThreads);
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -147,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto q_stage = [&](int st) { return smem + L::OFF_QD + (2 * st) * L::TILE_Q; };
     auto do_stage = [&](int st) { return smem + L::OFF_QD + (2 * st + 1) * L::TILE_Q; };
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q);
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_drain(&qd_full[t % QS], (t / QS) & 1, 10000000ull);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t fmt = BF16 ? 1u : 0u;
@@ -212,13 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dok_desc0 = make_sdesc_sw128(smem_u32(do_stage(0)), 16, 1024);
             const uint64_t qm_desc0 = make_sdesc_sw128(smem_u32(q_stage(0)), L::BOX_Q, 1024);    // MN-major
             const uint64_t dom_desc0 = make_sdesc_sw128(smem_u32(do_stage(0)), L::BOX_Q, 1024);
-            const uint64_t ds_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_DS), 0, 1024);
+            // dS^T rows of 128 queries = two 64-query boxes (MN-major B, LBO = box stride)
+            const uint64_t ds_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_DS), L::DS_BOX, 1024);
             constexpr uint32_t kStage = 2 * L::TILE_Q;  // bytes between Q/dO stages
             bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 22);
 
-            // S^T = K_j Q_t^T and dP^T = V_j dO_t^T into tensor-memory buffer t % 2
+            // S^T = K_j Q_t^T -> [0, 128) and dP^T = V_j dO_t^T -> [128, 256)
             auto issue_sdp = [&](int t) -> bool {
-                const int bb = t & 1;
                 const int st = t % QS;
                 if (!mbar_wait(&qd_full[st], (t / QS) & 1, abort_flag, p.status, 23)) return false;
                 tc_fence_after();
@@ -228,53 +235,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
                     const uint32_t oq = (kk >> 2) * L::BOX_Q + (kk & 3) * 32;
-                    mma_f16_ss(tmem + bb * 128, sdesc_advance(k_desc, okv), sdesc_advance(q_desc, oq), idesc_sdp,
+                    mma_f16_ss(tmem + kColS, sdesc_advance(k_desc, okv), sdesc_advance(q_desc, oq), idesc_sdp,
                                kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
                     const uint32_t oq = (kk >> 2) * L::BOX_Q + (kk & 3) * 32;
-                    mma_f16_ss(tmem + bb * 128 + 64, sdesc_advance(v_desc, okv), sdesc_advance(do_desc, oq),
-                               idesc_sdp, kk > 0 ? 1u : 0u);
+                    mma_f16_ss(tmem + kColDP, sdesc_advance(v_desc, okv), sdesc_advance(do_desc, oq), idesc_sdp,
+                               kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&sdp_full[bb]);
+                mma_commit(sdp_full);
                 return true;
             };
 
             if (ok) ok = issue_sdp(0);
-            if (ok && n_it > 1) ok = issue_sdp(1);
             for (int it = 0; ok && it < n_it; ++it) {
-                const int bb = it & 1;
                 const int st = it % QS;
-                if (!mbar_wait(&ds_ready[bb], (it >> 1) & 1, abort_flag, p.status, 24)) { ok = false; break; }
+                if (!mbar_wait(ds_ready, it & 1, abort_flag, p.status, 24)) { ok = false; break; }
                 tc_fence_after();
-                const uint64_t ds_desc = sdesc_advance(ds_desc0, bb * L::DS_BYTES);
-                // dQ_i^T = K_j^T dS_i^T: A = K^T (head dim contiguous: MN-major), B = dS^T
-                // rows of keys in shared memory (MN-major); 16 keys = 2048 bytes per step
+                // dQ_i^T = K_j^T dS_i^T -> [128, 256) (lane = head-dim index);
+                // 16 keys = 16 rows = 2048 bytes of both operands per step
 #pragma unroll
                 for (int kk = 0; kk < kBKV / 16; ++kk)
-                    mma_f16_ss(tmem + bb * 128 + 64, sdesc_advance(kt_desc, kk * 2048),
-                               sdesc_advance(ds_desc, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
-                mma_commit(&dq_full[bb]);
+                    mma_f16_ss(tmem + kColDQ, sdesc_advance(kt_desc, kk * 2048), sdesc_advance(ds_desc, kk * 2048),
+                               idesc_dq, kk > 0 ? 1u : 0u);
+                mma_commit(dq_full);
                 const uint64_t qm_desc = sdesc_advance(qm_desc0, st * kStage);
                 const uint64_t dom_desc = sdesc_advance(dom_desc0, st * kStage);
                 const uint32_t acc_first = it > 0 ? 1u : 0u;
-                // dV_j += P^T dO_i and dK_j += dS^T Q_i (A from tensor memory)
+                // dV_j += P^T dO_i and dK_j += dS^T Q_i (A from tensor memory;
+                // 16 queries = 8 packed columns of A, 16 rows of B per step).
+                // Queries 32 m .. 32 m + 31 have P^T at columns 32 m .. + 15 and
+                // dS^T at 32 m + 16 .. + 31 (see the softmax warps).
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDV, tmem + bb * 128 + kk * 8, sdesc_advance(dom_desc, kk * 2048),
-                               idesc_acc, kk > 0 ? 1u : acc_first);
+                    mma_f16_ts(tmem + kColDV, tmem + kColS + (kk >> 1) * 32 + (kk & 1) * 8,
+                               sdesc_advance(dom_desc, kk * 2048), idesc_acc, kk > 0 ? 1u : acc_first);
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDK, tmem + bb * 128 + 32 + kk * 8, sdesc_advance(qm_desc, kk * 2048),
-                               idesc_acc, kk > 0 ? 1u : acc_first);
+                    mma_f16_ts(tmem + kColDK, tmem + kColS + (kk >> 1) * 32 + (kk & 1) * 8 + 16,
+                               sdesc_advance(qm_desc, kk * 2048), idesc_acc, kk > 0 ? 1u : acc_first);
                 mma_commit(&qd_empty[st]);
-                if (it + 2 < n_it) {
-                    // buffer bb is reused once dQ_i^T has been read out of it
-                    if (!mbar_wait(&dq_free[bb], (it >> 1) & 1, abort_flag, p.status, 25)) { ok = false; break; }
+                if (it + 1 < n_it) {
+                    // S^T / dP^T of the next tile overwrite P^T, dS^T (read by the MMAs
+                    // just issued, which run first) and dQ^T (read out once dq_free flips)
+                    if (!mbar_wait(dq_free, it & 1, abort_flag, p.status, 25)) { ok = false; break; }
                     tc_fence_after();
-                    if (!issue_sdp(it + 2)) { ok = false; break; }
+                    if (!issue_sdp(it + 1)) { ok = false; break; }
                 }
             }
             if (ok) mma_commit(acc_done);
@@ -283,170 +291,136 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_drain(drain, 0, 100000000ull);
         }
         __syncwarp();
-    } else if (warp < 4 || warp >= 10) {
-        // ------------------------------------------- softmax: P^T and dS^T
-        // Eight warps: warp w covers key rows 32 (w % 4) .. + 31 (its TMEM
-        // lane quarter) and query columns 32 hf .. + 31 of the Q tile.
-        const int hf = warp < 4 ? 0 : 1;
+    } else {
+        // --------------------- warps 0-7: softmax (P^T, dS^T), dQ read-out
+        // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
+        // query columns 64 hf .. + 63 (hf = w / 4), in two chunks of 32.
+        const int hf = warp >> 2;
         const int quarter = warp & 3;
-        const int c = quarter * 32 + lane;  // key row within the tile == TMEM lane
+        const int c = quarter * 32 + lane;  // key row == TMEM lane (== head-dim index for dQ^T)
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const float sl2 = p.scale_log2;
         const int kv = kv0 + c;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
-            const int bb = it & 1;
             const int st = it % QS;
             // every lane waits, then the warp votes: the tcgen05.ld/st below
             // are warp-collective and need all 32 lanes
-            const bool w1 = mbar_wait(&sdp_full[bb], (it >> 1) & 1, abort_flag, p.status, 26);
+            const bool w1 = mbar_wait(sdp_full, it & 1, abort_flag, p.status, 26);
             const bool w2 = w1 && mbar_wait(&qd_full[st], (it / QS) & 1, abort_flag, p.status, 27);
             if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
             tc_fence_after();
-            uint32_t s[32], dp[32];
-            tmem_ld_x32(lane_base + bb * 128 + hf * 32, s);
-            tmem_ld_x32(lane_base + bb * 128 + 64 + hf * 32, dp);
-            tmem_ld_wait_x32(s);
-            tmem_ld_wait_x32(dp);
-            const float *l2s = ld_smem + st * 2 * kBQ + hf * 32;
-            const float *dsm = ld_smem + st * 2 * kBQ + kBQ + hf * 32;
-            const int q_first = (i_start + it % n_i) * kBQ + hf * 32;
-            const bool diag = p.causal && (q_first < kv0 + kBKV);
-            uint32_t pp[16], dd[16];
+            const int q_base = (i_start + it % n_i) * kBQ;
+            const bool diag = p.causal && (q_base + hf * 64 < kv0 + kBKV);
+            uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
 #pragma unroll
-            for (int r = 0; r < 32; r += 2) {
-                const float2 lv = *reinterpret_cast<const float2 *>(l2s + r);
-                const float2 dv = *reinterpret_cast<const float2 *>(dsm + r);
-                float p0 = ex2_approx(fmaf(__uint_as_float(s[r]), sl2, -lv.x));
-                float p1 = ex2_approx(fmaf(__uint_as_float(s[r + 1]), sl2, -lv.y));
-                if (diag) {  // causal: key kv is visible to query q iff kv <= q
-                    if (kv > q_first + r) p0 = 0.0f;
-                    if (kv > q_first + r + 1) p1 = 0.0f;
+            for (int ch = 0; ch < 2; ++ch) {
+                const int qc = hf * 64 + ch * 32;  // first query column of this chunk
+                uint32_t s[32], dp[32];
+                tmem_ld_x32(lane_base + kColS + qc, s);
+                tmem_ld_x32(lane_base + kColDP + qc, dp);
+                tmem_ld_wait_x32(s);
+                tmem_ld_wait_x32(dp);
+                const float *l2s = ld_smem + st * 2 * kBQ + qc;
+                const float *dsm = ld_smem + st * 2 * kBQ + kBQ + qc;
+                const int q_first = q_base + qc;
+                uint32_t pp[16], dd[16];
+#pragma unroll
+                for (int r = 0; r < 32; r += 2) {
+                    const float2 lv = *reinterpret_cast<const float2 *>(l2s + r);
+                    const float2 dv = *reinterpret_cast<const float2 *>(dsm + r);
+                    float p0 = ex2_approx(fmaf(__uint_as_float(s[r]), sl2, -lv.x));
+                    float p1 = ex2_approx(fmaf(__uint_as_float(s[r + 1]), sl2, -lv.y));
+                    if (diag) {  // causal: key kv is visible to query q iff kv <= q
+                        if (kv > q_first + r) p0 = 0.0f;
+                        if (kv > q_first + r + 1) p1 = 0.0f;
+                    }
+                    const float d0 = p0 * (__uint_as_float(dp[r]) - dv.x);
+                    const float d1 = p1 * (__uint_as_float(dp[r + 1]) - dv.y);
+                    if constexpr (BF16) {
+                        pp[r / 2] = pack_bf16x2(p0, p1);
+                        dd[r / 2] = pack_bf16x2(d0, d1);
+                    } else {
+                        pp[r / 2] = pack_f16x2(p0, p1);
+                        dd[r / 2] = pack_f16x2(d0, d1);
+                    }
                 }
-                const float d0 = p0 * (__uint_as_float(dp[r]) - dv.x);
-                const float d1 = p1 * (__uint_as_float(dp[r + 1]) - dv.y);
-                if constexpr (BF16) {
-                    pp[r / 2] = pack_bf16x2(p0, p1);
-                    dd[r / 2] = pack_bf16x2(d0, d1);
-                } else {
-                    pp[r / 2] = pack_f16x2(p0, p1);
-                    dd[r / 2] = pack_f16x2(d0, d1);
-                }
+                __syncwarp();
+                // P^T and dS^T of this chunk go into the chunk's own S^T columns
+                // [qc, qc + 32), which this warp has just read and no other warp
+                // reads: P^T at qc .. qc + 15, dS^T at qc + 16 .. qc + 31
+                tmem_st_x16(lane_base + kColS + qc, pp);
+                tmem_st_x16(lane_base + kColS + qc + 16, dd);
+                // dS^T row c, queries qc .. qc + 31 -> chunks 4 ch .. 4 ch + 3 of
+                // the 128-byte swizzled row of box hf
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4 *>(ds_row + (((4 * ch + q) ^ (c & 7)) << 4)) =
+                        make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
             }
-            __syncwarp();
-            tmem_st_x16(lane_base + bb * 128 + hf * 16, pp);
-            tmem_st_x16(lane_base + bb * 128 + 32 + hf * 16, dd);
-            // dS^T row c, query columns 32 hf .. + 31 -> shared memory (the
-            // 128-byte swizzled row of 64 values; this warp writes chunks 4 hf .. + 3)
-            uint8_t *row = smem + L::OFF_DS + bb * L::DS_BYTES + c * 128;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4 *>(row + (((4 * hf + q) ^ (c & 7)) << 4)) =
-                    make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
             fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&ds_ready[bb]);
-        }
-        // ------------------------------------------------- dV epilogue
-        if (warp < 4) {
-            bool ok2 = ok && mbar_wait(acc_done, 0, abort_flag, p.status, 28);
-            __syncwarp();
-            ok2 = named_bar_and(1, 128, ok2);
-            if (ok2) {
-                tc_fence_after();
-                uint8_t *stage = q_stage(0);  // idle after the last MMA
-#pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld_x32(lane_base + kColDV + c0, o);
-                    tmem_ld_wait_x32(o);
-                    uint32_t wv[16];
-#pragma unroll
-                    for (int x = 0; x < 16; ++x)
-                        wv[x] = BF16 ? pack_bf16x2(__uint_as_float(o[2 * x]), __uint_as_float(o[2 * x + 1]))
-                                     : pack_f16x2(__uint_as_float(o[2 * x]), __uint_as_float(o[2 * x + 1]));
-                    uint8_t *rowp = stage + (c0 >> 6) * L::BOX_KV + c * 128;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int chunk = ((c0 & 63) >> 3) + q;
-                        *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (c & 7)) << 4)) =
-                            make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
-                    }
-                }
-                fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (c == 0) {
-                    for (int bx = 0; bx < L::NBOX; ++bx)
-                        tma_store_3d(&tm_dv, stage + bx * L::BOX_KV, bx * 64, kv0, bg);
-                    bulk_commit();
-                    bulk_wait_read_all();
-                }
-            }
-        }
-        __syncwarp();
-    } else {
-        // --------------------------------- dQ read-out and atomic reduction
-        // warps 6..9: thread t = TMEM lane = head-dim index of dQ^T
-        const int t = (warp & 3) * 32 + lane;
-        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        bool ok = true;
-        for (int it = 0; it < n_it; ++it) {
-            const int bb = it & 1;
-            const bool got = mbar_wait(&dq_full[bb], (it >> 1) & 1, abort_flag, p.status, 29);
+            mbar_arrive(ds_ready);
+
+            // dQ^T read-out: lane = head-dim index t = c, columns = queries
+            const bool got = mbar_wait(dq_full, it & 1, abort_flag, p.status, 29);
             if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
             tc_fence_after();
             uint32_t v[64];
-            tmem_ld_x32(lane_base + bb * 128 + 64, v);
-            tmem_ld_x32(lane_base + bb * 128 + 96, v + 32);
+            tmem_ld_x32(lane_base + kColDQ + hf * 64, v);
+            tmem_ld_x32(lane_base + kColDQ + hf * 64 + 32, v + 32);
             tmem_ld_wait_x32(v);
             tmem_ld_wait_x32(v + 32);
             tc_fence_before();
-            mbar_arrive(&dq_free[bb]);
+            mbar_arrive(dq_free);
             const int h = g * G + it / n_i;
-            const int q_base = (i_start + it % n_i) * kBQ;
-            const int rows = min(kBQ, p.N - q_base);
-            if (t < D) {
-                // element (q_base + r, t) of this head's dQ: consecutive lanes
-                // touch consecutive floats (one 128-byte line per warp and row)
-                float *dst = p.dq_acc + ((size_t)(b * p.Hq + h) * p.N + q_base) * D + t;
+            const int rows = min(64, p.N - (q_base + hf * 64));
+            if (c < D) {
+                // element (q, c) of this head's dQ: consecutive lanes touch
+                // consecutive floats (one 128-byte line per warp and row)
+                float *dst = p.dq_acc + ((size_t)(b * p.Hq + h) * p.N + q_base + hf * 64) * D + c;
 #pragma unroll
-                for (int r = 0; r < kBQ; ++r)
+                for (int r = 0; r < 64; ++r)
                     if (r < rows) atomicAdd(dst + (size_t)r * D, __uint_as_float(v[r]));
             }
         }
-        // ------------------------------------------------- dK epilogue
-        bool ok2 = ok && mbar_wait(acc_done, 0, abort_flag, p.status, 30);
+        // ------------------------------- epilogue: dV (warps 0-3), dK (warps 4-7)
+        bool ok2 = ok && mbar_wait(acc_done, 0, abort_flag, p.status, 28);
         __syncwarp();
-        ok2 = named_bar_and(2, 128, ok2);
+        ok2 = named_bar_and(1 + hf, 128, ok2);
         if (ok2) {
             tc_fence_after();
-            uint8_t *stage = q_stage(1);
+            // the first Q/dO stage is idle after the last MMA: dV goes to its Q
+            // buffer, dK to its dO buffer
+            uint8_t *stage = hf == 0 ? q_stage(0) : do_stage(0);
+            const uint32_t col = hf == 0 ? kColDV : kColDK;
+            const float f = hf == 0 ? 1.0f : p.scale;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
-                tmem_ld_x32(lane_base + kColDK + c0, o);
+                tmem_ld_x32(lane_base + col + c0, o);
                 tmem_ld_wait_x32(o);
-                uint32_t wk[16];
+                uint32_t w[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    const float a0 = __uint_as_float(o[2 * x]) * p.scale;
-                    const float a1 = __uint_as_float(o[2 * x + 1]) * p.scale;
-                    wk[x] = BF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
+                    const float a0 = __uint_as_float(o[2 * x]) * f;
+                    const float a1 = __uint_as_float(o[2 * x + 1]) * f;
+                    w[x] = BF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
                 }
-                uint8_t *rowp = stage + (c0 >> 6) * L::BOX_KV + t * 128;
+                uint8_t *rowp = stage + (c0 >> 6) * L::BOX_KV + c * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int chunk = ((c0 & 63) >> 3) + q;
-                    *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (t & 7)) << 4)) =
-                        make_uint4(wk[4 * q], wk[4 * q + 1], wk[4 * q + 2], wk[4 * q + 3]);
+                    *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (c & 7)) << 4)) =
+                        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
                 }
             }
             fence_proxy_async_smem();
-            named_bar_sync(2, 128);
-            if (t == 0) {
-                for (int bx = 0; bx < L::NBOX; ++bx)
-                    tma_store_3d(&tm_dk, stage + bx * L::BOX_KV, bx * 64, kv0, bg);
+            named_bar_sync(1 + hf, 128);
+            if (c == 0) {
+                const CUtensorMap *tm = hf == 0 ? &tm_dv : &tm_dk;
+                for (int bx = 0; bx < L::NBOX; ++bx) tma_store_3d(tm, stage + bx * L::BOX_KV, bx * 64, kv0, bg);
                 bulk_commit();
                 bulk_wait_read_all();
             }
@@ -456,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
