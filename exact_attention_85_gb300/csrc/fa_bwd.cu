@@ -20,18 +20,19 @@
 // 128 rows, so every MMA is 128 x 128 (full tensor-core rate; at 64 columns the
 // shared-memory operand traffic caps the rate near two thirds).  Tensor
 // memory (512 columns, fp32, lane = key row unless noted):
-//   [0, 128)   S^T = K_j Q_i^T    -> then, per 32-query chunk m, P^T in
-//              [32 m, 32 m + 16) and dS^T in [32 m + 16, 32 m + 32) (16-bit pairs)
+//   [0, 128)   S^T = K_j Q_i^T    -> then, per 16-query chunk m, P^T in
+//              [16 m, 16 m + 8) and dS^T in [16 m + 8, 16 m + 16) (16-bit pairs)
 //   [128, 256) dP^T = V_j dO_i^T  -> then dQ_i^T = K_j^T dS_i^T (lane = head-dim index)
 //   [256, 256 + d) dV_j,  [384, 384 + d) dK_j  (accumulated over all Q tiles)
 // P^T and dS^T stay in tensor memory as the A operands of dV += P^T dO and
 // dK += dS^T Q; dS^T is also written to shared memory as the B operand of
 // dQ^T = K^T dS^T.  Per Q tile: MMA S^T, dP^T -> softmax warps -> MMA dQ^T,
-// dV, dK -> the same warps read dQ^T out (which frees the columns for the next
-// S^T, dP^T) and add it into dQacc with fp32 atomic reductions (one 128-byte
-// line per warp and query row) while the tensor cores run on.
-// Warps: 0-7 softmax + dQ read-out (then 0-3 store dV, 4-7 store dK),
-// 8 TMA producer (Q / dO through a 2-deep ring), 9 MMA issuer + TMEM owner.
+// dV, dK -> read-out warps copy dQ^T out of tensor memory (which frees the
+// columns for the next S^T, dP^T) and add it into dQacc with fp32 atomic
+// reductions (one 128-byte line per warp and query row) while the softmax
+// warps already work on the next tile.
+// Warps: 0-7 softmax (then 0-3 store dV, 4-7 store dK), 8-15 dQ read-out,
+// 16 TMA producer (Q / dO through a 2-deep ring), 17 MMA issuer + TMEM owner.
 #include "host_util.h"
 #include "ptx.cuh"
 
@@ -41,8 +42,10 @@ namespace {
 
 constexpr int kBQ = 128;       // query rows per Q tile
 constexpr int kBKV = 128;      // key rows per CTA (TMEM lanes)
-constexpr int kThreads = 320;  // 10 warps
-constexpr int kWorkThreads = 256;  // warps 0-7: softmax, dQ read-out, epilogue
+constexpr int kThreads = 576;  // 18 warps
+constexpr int kSoftmaxThreads = 256;  // warps 0-7
+constexpr int kReadoutThreads = 256;  // warps 8-15
+constexpr int kProducerWarp = 16, kMmaWarp = 17;
 
 template <int D>
 struct BwdLayout {
@@ -134,15 +137,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&qd_empty[s], 1);
         }
         mbar_init(sdp_full, 1);
-        mbar_init(ds_ready, kWorkThreads);
+        mbar_init(ds_ready, kSoftmaxThreads);
         mbar_init(dq_full, 1);
-        mbar_init(dq_free, kWorkThreads);
+        mbar_init(dq_free, kReadoutThreads);
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto q_stage = [&](int st) { return smem + L::OFF_QD + (2 * st) * L::TILE_Q; };
     auto do_stage = [&](int st) { return smem + L::OFF_QD + (2 * st + 1) * L::TILE_Q; };
 
-    if (warp == 8) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q);
@@ -189,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int r = lane; r < kBQ; r += 32) {
                 const int row = q_base + r;
                 const bool in = row < p.N;
-                // rows past N: L = +inf makes P = 0 for them
-                l2s[r] = in ? p.lse[(size_t)plane * p.N + row] * 1.4426950408889634f : INFINITY;
+                // stored negated in log2 units; rows past N get -inf, so P = 0
+                l2s[r] = in ? -p.lse[(size_t)plane * p.N + row] * 1.4426950408889634f : -INFINITY;
                 dsm[r] = in ? p.Dvec[(size_t)plane * p.N + row] : 0.0f;
             }
             mbar_arrive(&qd_full[st]);  // releases this lane's L / D writes
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait_drain(&qd_full[t % QS], (t / QS) & 1, 10000000ull);
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t fmt = BF16 ? 1u : 0u;
@@ -266,16 +269,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t acc_first = it > 0 ? 1u : 0u;
                 // dV_j += P^T dO_i and dK_j += dS^T Q_i (A from tensor memory;
                 // 16 queries = 8 packed columns of A, 16 rows of B per step).
-                // Queries 32 m .. 32 m + 31 have P^T at columns 32 m .. + 15 and
-                // dS^T at 32 m + 16 .. + 31 (see the softmax warps).
+                // Queries 16 m .. 16 m + 15 have P^T at columns 16 m .. + 7 and
+                // dS^T at 16 m + 8 .. + 15 (see the softmax warps).
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDV, tmem + kColS + (kk >> 1) * 32 + (kk & 1) * 8,
-                               sdesc_advance(dom_desc, kk * 2048), idesc_acc, kk > 0 ? 1u : acc_first);
+                    mma_f16_ts(tmem + kColDV, tmem + kColS + kk * 16, sdesc_advance(dom_desc, kk * 2048), idesc_acc,
+                               kk > 0 ? 1u : acc_first);
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDK, tmem + kColS + (kk >> 1) * 32 + (kk & 1) * 8 + 16,
-                               sdesc_advance(qm_desc, kk * 2048), idesc_acc, kk > 0 ? 1u : acc_first);
+                    mma_f16_ts(tmem + kColDK, tmem + kColS + kk * 16 + 8, sdesc_advance(qm_desc, kk * 2048),
+                               idesc_acc, kk > 0 ? 1u : acc_first);
                 mma_commit(&qd_empty[st]);
                 if (it + 1 < n_it) {
                     // S^T / dP^T of the next tile overwrite P^T, dS^T (read by the MMAs
@@ -291,15 +294,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_drain(drain, 0, 100000000ull);
         }
         __syncwarp();
-    } else {
-        // --------------------- warps 0-7: softmax (P^T, dS^T), dQ read-out
+    } else if (warp < 8) {
+        // ----------------------------------- warps 0-7: softmax (P^T, dS^T)
         // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
-        // query columns 64 hf .. + 63 (hf = w / 4), in two chunks of 32.
+        // query columns 64 hf .. + 63 (hf = w / 4), in four chunks of 16.
         const int hf = warp >> 2;
         const int quarter = warp & 3;
-        const int c = quarter * 32 + lane;  // key row == TMEM lane (== head-dim index for dQ^T)
+        const int c = quarter * 32 + lane;  // key row == TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const float sl2 = p.scale_log2;
+        const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
         const int kv = kv0 + c;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
@@ -314,76 +317,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool diag = p.causal && (q_base + hf * 64 < kv0 + kBKV);
             uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const int qc = hf * 64 + ch * 32;  // first query column of this chunk
-                uint32_t s[32], dp[32];
-                tmem_ld_x32(lane_base + kColS + qc, s);
-                tmem_ld_x32(lane_base + kColDP + qc, dp);
-                tmem_ld_wait_x32(s);
-                tmem_ld_wait_x32(dp);
-                const float *l2s = ld_smem + st * 2 * kBQ + qc;
-                const float *dsm = ld_smem + st * 2 * kBQ + kBQ + qc;
+            for (int ch = 0; ch < 4; ++ch) {
+                const int qc = hf * 64 + ch * 16;  // first query column of this chunk
+                uint32_t s[16], dp[16];
+                tmem_ld_x16(lane_base + kColS + qc, s);
+                tmem_ld_x16(lane_base + kColDP + qc, dp);
+                tmem_ld_wait_x16(s);
+                tmem_ld_wait_x16(dp);
+                const float *nl2 = ld_smem + st * 2 * kBQ + qc;          // -L log2(e)
+                const float *dsm = ld_smem + st * 2 * kBQ + kBQ + qc;    // D
                 const int q_first = q_base + qc;
-                uint32_t pp[16], dd[16];
+                uint32_t pp[8], dd[8];
 #pragma unroll
-                for (int r = 0; r < 32; r += 2) {
-                    const float2 lv = *reinterpret_cast<const float2 *>(l2s + r);
-                    const float2 dv = *reinterpret_cast<const float2 *>(dsm + r);
-                    float p0 = ex2_approx(fmaf(__uint_as_float(s[r]), sl2, -lv.x));
-                    float p1 = ex2_approx(fmaf(__uint_as_float(s[r + 1]), sl2, -lv.y));
+                for (int r = 0; r < 16; r += 2) {
+                    const float2 x = ffma2(make_float2(__uint_as_float(s[r]), __uint_as_float(s[r + 1])), sl2,
+                                           *reinterpret_cast<const float2 *>(nl2 + r));
+                    float p0 = ex2_approx(x.x);
+                    float p1 = ex2_approx(x.y);
                     if (diag) {  // causal: key kv is visible to query q iff kv <= q
                         if (kv > q_first + r) p0 = 0.0f;
                         if (kv > q_first + r + 1) p1 = 0.0f;
                     }
-                    const float d0 = p0 * (__uint_as_float(dp[r]) - dv.x);
-                    const float d1 = p1 * (__uint_as_float(dp[r + 1]) - dv.y);
+                    const float2 t = fsub2(make_float2(__uint_as_float(dp[r]), __uint_as_float(dp[r + 1])),
+                                           *reinterpret_cast<const float2 *>(dsm + r));
+                    const float2 ds = fmul2(make_float2(p0, p1), t);
                     if constexpr (BF16) {
                         pp[r / 2] = pack_bf16x2(p0, p1);
-                        dd[r / 2] = pack_bf16x2(d0, d1);
+                        dd[r / 2] = pack_bf16x2(ds.x, ds.y);
                     } else {
                         pp[r / 2] = pack_f16x2(p0, p1);
-                        dd[r / 2] = pack_f16x2(d0, d1);
+                        dd[r / 2] = pack_f16x2(ds.x, ds.y);
                     }
                 }
                 __syncwarp();
                 // P^T and dS^T of this chunk go into the chunk's own S^T columns
-                // [qc, qc + 32), which this warp has just read and no other warp
-                // reads: P^T at qc .. qc + 15, dS^T at qc + 16 .. qc + 31
-                tmem_st_x16(lane_base + kColS + qc, pp);
-                tmem_st_x16(lane_base + kColS + qc + 16, dd);
-                // dS^T row c, queries qc .. qc + 31 -> chunks 4 ch .. 4 ch + 3 of
-                // the 128-byte swizzled row of box hf
+                // [qc, qc + 16), which this warp has just read and no other warp
+                // reads: P^T at qc .. qc + 7, dS^T at qc + 8 .. qc + 15
+                tmem_st_x8(lane_base + kColS + qc, pp);
+                tmem_st_x8(lane_base + kColS + qc + 8, dd);
+                // dS^T row c, queries qc .. qc + 15 -> 16-byte chunks 2 ch, 2 ch + 1
+                // of the 128-byte swizzled row of box hf
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4 *>(ds_row + (((4 * ch + q) ^ (c & 7)) << 4)) =
+                for (int q = 0; q < 2; ++q)
+                    *reinterpret_cast<uint4 *>(ds_row + (((2 * ch + q) ^ (c & 7)) << 4)) =
                         make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
             }
             fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(ds_ready);
-
-            // dQ^T read-out: lane = head-dim index t = c, columns = queries
-            const bool got = mbar_wait(dq_full, it & 1, abort_flag, p.status, 29);
-            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t v[64];
-            tmem_ld_x32(lane_base + kColDQ + hf * 64, v);
-            tmem_ld_x32(lane_base + kColDQ + hf * 64 + 32, v + 32);
-            tmem_ld_wait_x32(v);
-            tmem_ld_wait_x32(v + 32);
-            tc_fence_before();
-            mbar_arrive(dq_free);
-            const int h = g * G + it / n_i;
-            const int rows = min(64, p.N - (q_base + hf * 64));
-            if (c < D) {
-                // element (q, c) of this head's dQ: consecutive lanes touch
-                // consecutive floats (one 128-byte line per warp and row)
-                float *dst = p.dq_acc + ((size_t)(b * p.Hq + h) * p.N + q_base + hf * 64) * D + c;
-#pragma unroll
-                for (int r = 0; r < 64; ++r)
-                    if (r < rows) atomicAdd(dst + (size_t)r * D, __uint_as_float(v[r]));
-            }
         }
         // ------------------------------- epilogue: dV (warps 0-3), dK (warps 4-7)
         bool ok2 = ok && mbar_wait(acc_done, 0, abort_flag, p.status, 28);
@@ -426,11 +408,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else {
+        // ------------------- warps 8-15: dQ^T read-out and atomic reduction
+        // Warp w reads TMEM lane quarter w % 4 (lane = head-dim index t) and
+        // query columns 64 hf .. + 63 (hf = (w - 8) / 4).
+        const int hf = (warp - 8) >> 2;
+        const int quarter = warp & 3;
+        const int t = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        for (int it = 0; it < n_it; ++it) {
+            const bool got = mbar_wait(dq_full, it & 1, abort_flag, p.status, 29);
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            uint32_t v[64];
+            tmem_ld_x32(lane_base + kColDQ + hf * 64, v);
+            tmem_ld_x32(lane_base + kColDQ + hf * 64 + 32, v + 32);
+            tmem_ld_wait_x32(v);
+            tmem_ld_wait_x32(v + 32);
+            tc_fence_before();
+            mbar_arrive(dq_free);
+            const int h = g * G + it / n_i;
+            const int q_first = (i_start + it % n_i) * kBQ + hf * 64;
+            const int rows = min(64, p.N - q_first);
+            if (t < D) {
+                // element (q, t) of this head's dQ: consecutive lanes touch
+                // consecutive floats (one 128-byte line per warp and row)
+                float *dst = p.dq_acc + ((size_t)(b * p.Hq + h) * p.N + q_first) * D + t;
+#pragma unroll
+                for (int r = 0; r < 64; ++r)
+                    if (r < rows) atomicAdd(dst + (size_t)r * D, __uint_as_float(v[r]));
+            }
+        }
+        __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
