@@ -19,8 +19,11 @@
 //                    limit), then the epilogue.
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128) S buffer 0   [128,256) S buffer 1   [256,256+d) O accumulator
-//   [384,448) P buffer 0 [448,512) P buffer 1  (P: 16-bit pairs, the A
-//   operand of the P.V MMA read straight from TMEM)
+//   [384,384+d/2) Q (16-bit pairs, the A operand of S = Q K^T, copied once)
+// P (16-bit pairs) overwrites the first 64 columns of its own S buffer (each
+// softmax thread writes only its own lane, after reading the whole row) and is
+// the A operand of the P.V MMA.  With Q and P read from tensor memory only K
+// and V occupy the shared-memory operand path (128 bytes / cycle).
 // Pipeline per K/V tile j: MMA S_j = Q K_j^T -> softmax_j (P_j, row stats)
 // -> MMA O += P_j V_j.  S is double-buffered so S_{j+1} runs on the tensor
 // cores while softmax_j runs, and softmax_{j+1} overlaps O += P_j V_j.
@@ -53,9 +56,9 @@ struct FwdLayout {
     static constexpr int OFF_K = OFF_Q + TILE_Q;
     static constexpr int OFF_V = OFF_K + KS * TILE_KV;
     static constexpr int OFF_BAR = OFF_V + VS * TILE_KV;
-    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
-    // p_full[2], o_done, drain
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 + 2 + 1 + 1;
+    // q_full, q_tmem, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
+    // s_full[2], p_full[2], o_done, drain
+    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 2 + 1 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
@@ -68,7 +71,7 @@ struct FwdParams {
     float scale_log2;  // scale * log2(e)
 };
 
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -80,7 +83,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *q_full = bars;
-    uint64_t *k_full = q_full + 1;
+    uint64_t *q_tmem = bars + 1;
+    uint64_t *k_full = q_tmem + 1;
     uint64_t *k_empty = k_full + L::KS;
     uint64_t *v_full = k_empty + L::KS;
     uint64_t *v_empty = v_full + L::VS;
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_tmem, kBM);
         for (int s = 0; s < L::KS; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
         for (int s = 0; s < L::VS; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
         for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&p_full[s], kBM); }
@@ -178,10 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_s = make_idesc(kBM, kBN, fmt, false, false);
             constexpr uint32_t idesc_pv = make_idesc(kBM, D, fmt, false, true);
             // one descriptor per operand tile; steps are derived by sdesc_advance
-            const uint64_t q_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_Q), 16, 1024);
             const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);
             const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_V), kBN * 128, 1024);
-            bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 3);
+            // Q is in tensor memory once the softmax warps have copied it
+            bool ok = mbar_wait(q_tmem, 0, abort_flag, p.status, 3);
+            tc_fence_after();
 
             auto issue_pv = [&](int t) -> bool {
                 const int pb = t & 1;
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&v_full[vs], (t / L::VS) & 1, abort_flag, p.status, 5)) return false;
                 tc_fence_after();
                 const uint64_t v_desc = sdesc_advance(v_desc0, vs * L::TILE_KV);
-                const uint32_t p_col = tmem + kColP + pb * 64;
+                const uint32_t p_col = tmem + kColS + pb * kBN;  // P overlays its S buffer
                 // B = V (N = d contiguous: MN-major); 16 keys = 16 rows of 128 B
                 mma_f16_ts(tmem + kColO, p_col, v_desc, idesc_pv, t > 0 ? 1u : 0u);
 #pragma unroll
@@ -207,11 +213,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint64_t k_desc = sdesc_advance(k_desc0, ks * L::TILE_KV);
                 const uint32_t s_col = tmem + kColS + (j & 1) * kBN;
+                // A = Q from tensor memory (16 head-dim values = 8 columns per
+                // step), B = K (K-major, 32 bytes per step inside a 128-byte row)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-                    mma_f16_ss(s_col, sdesc_advance(q_desc, off), sdesc_advance(k_desc, off), idesc_s,
-                               kk > 0 ? 1u : 0u);
+                    const uint32_t off = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
+                    mma_f16_ts(s_col, tmem + kColQ + kk * 8, sdesc_advance(k_desc, off), idesc_s, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&s_full[j & 1]);
                 mma_commit(&k_empty[ks]);
@@ -234,7 +241,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         uint32_t s[128];
 
-        for (int j = 0; j < nkv; ++j) {
+        {
+            // copy this row of Q from the swizzled shared tile into tensor memory
+            const bool got_q = mbar_wait(q_full, 0, abort_flag, p.status, 10);
+            ok = __all_sync(0xffffffffu, got_q);
+            if (ok) {
+                uint32_t qv[D / 2];
+#pragma unroll
+                for (int bx = 0; bx < L::NBOX; ++bx)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(smem + L::OFF_Q + bx * kBM * 128 + row * 128 +
+                                                                         ((k ^ (row & 7)) << 4));
+                        qv[bx * 32 + k * 4 + 0] = u.x;
+                        qv[bx * 32 + k * 4 + 1] = u.y;
+                        qv[bx * 32 + k * 4 + 2] = u.z;
+                        qv[bx * 32 + k * 4 + 3] = u.w;
+                    }
+#pragma unroll
+                for (int c0 = 0; c0 < D / 2; c0 += 32) tmem_st_x32(lane_base + kColQ + c0, qv + c0);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(q_tmem);
+            }
+        }
+
+        for (int j = 0; ok && j < nkv; ++j) {
             const int sb = j & 1;
             // every lane waits, then the warp votes: the tcgen05.ld/st below
             // are warp-collective (.sync.aligned) and need all 32 lanes
@@ -278,15 +310,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = mx;
                 rescale = true;
             }
-            const float neg_m = -m_ref;
-            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f, e0 = 0.f, e1 = 0.f;
+            const float2 neg_m = make_float2(-m_ref, -m_ref);
+            const float2 sl2x2 = make_float2(sl2, sl2);
+            float2 lr01 = make_float2(0.f, 0.f), lr23 = lr01, le01 = lr01, le23 = lr01;
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, neg_m));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, neg_m));
-                const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), sl2, neg_m));
-                const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), sl2, neg_m));
+                const float2 x01 = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, neg_m);
+                const float2 x23 =
+                    ffma2(make_float2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2, neg_m);
+                const float p0 = ex2_approx(x01.x);
+                const float p1 = ex2_approx(x01.y);
+                const float p2 = ex2_approx(x23.x);
+                const float p3 = ex2_approx(x23.y);
                 // l sums the rounded P that the MMA consumes, so O~ / l is an
                 // exactly normalised mix of V rows even when one term dominates
                 if constexpr (BF16) {
@@ -296,15 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[c / 2] = pack_f16x2(p0, p1);
                     pk[c / 2 + 1] = pack_f16x2(p2, p3);
                 }
-                const float2 r01 = unpack2<BF16>(pk[c / 2]);
-                const float2 r23 = unpack2<BF16>(pk[c / 2 + 1]);
-                l0 += r01.x; l1 += r01.y; l2 += r23.x; l3 += r23.y;
-                e0 += p0 + p1; e1 += p2 + p3;
+                lr01 = fadd2(lr01, unpack2<BF16>(pk[c / 2]));
+                lr23 = fadd2(lr23, unpack2<BF16>(pk[c / 2 + 1]));
+                le01 = fadd2(le01, make_float2(p0, p1));
+                le23 = fadd2(le23, make_float2(p2, p3));
             }
-            l_sum += (l0 + l1) + (l2 + l3);
-            l_exact += e0 + e1;
+            l_sum += (lr01.x + lr01.y) + (lr23.x + lr23.y);
+            l_exact += (le01.x + le01.y) + (le23.x + le23.y);
             __syncwarp();  // reconverge after the per-row branches above
-            const uint32_t p_addr = lane_base + kColP + sb * 64;
+            const uint32_t p_addr = lane_base + kColS + sb * kBN;  // P overlays the S row just read
             tmem_st_x32(p_addr, pk);
             tmem_st_x32(p_addr + 32, pk + 32);
 
