@@ -182,7 +182,7 @@ struct Fp8Layout {
     static constexpr int OFF_V = OFF_K + KS * TILE;
     static constexpr int OFF_O = OFF_V + VS * TILE;  // bf16 output staging, 2 boxes of 128 x 64
     static constexpr int OFF_BAR = OFF_O + kBM * kD * 2;
-    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 + 2 + 1 + 1;
+    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 2 + 1 + 1;  // + q_tmem
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;
@@ -196,7 +196,9 @@ struct Fp8Params {
     float scale_log2;
 };
 
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;  // P buffers: 32 columns each
+// S buffers [0,128), [128,256); O [256,384); Q [384,416) (4 e4m3 per column).
+// P (e4m3, 32 columns) overlays the first columns of its own S buffer.
+constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;
 
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -207,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *q_full = bars;
-    uint64_t *k_full = q_full + 1;
+    uint64_t *q_tmem = bars + 1;
+    uint64_t *k_full = q_tmem + 1;
     uint64_t *k_empty = k_full + L::KS;
     uint64_t *v_full = k_empty + L::KS;
     uint64_t *v_empty = v_full + L::VS;
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_tmem, kBM);
         for (int s = 0; s < L::KS; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
         for (int s = 0; s < L::VS; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
         for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&p_full[s], kBM); }
@@ -295,10 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // kind::f8f6f4, e4m3 (format 0) for both operands, fp32 accumulate
             constexpr uint32_t idesc_s = make_idesc(kBM, kBN, 0u, false, false);
             constexpr uint32_t idesc_pv = make_idesc(kBM, kD, 0u, false, true);
-            const uint64_t q_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_Q), 16, 1024);
             const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);
             const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_V), 0, 1024);
-            bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 43);
+            // Q is in tensor memory once the softmax warps have copied it
+            bool ok = mbar_wait(q_tmem, 0, abort_flag, p.status, 43);
+            tc_fence_after();
 
             auto issue_pv = [&](int t) -> bool {
                 const int pb = t & 1;
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&v_full[vs], (t / L::VS) & 1, abort_flag, p.status, 45)) return false;
                 tc_fence_after();
                 const uint64_t v_desc = sdesc_advance(v_desc0, vs * L::TILE);
-                const uint32_t p_col = tmem + kColP + pb * 32;
+                const uint32_t p_col = tmem + kColS + pb * kBN;  // P overlays its S buffer
                 // B = V: head dim contiguous (MN-major), 32 keys = 32 rows of 128 B
                 mma_f8_ts(tmem + kColO, p_col, v_desc, idesc_pv, t > 0 ? 1u : 0u);
 #pragma unroll
@@ -324,10 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint64_t k_desc = sdesc_advance(k_desc0, ks * L::TILE);
                 const uint32_t s_col = tmem + kColS + (j & 1) * kBN;
+                // A = Q from tensor memory (32 values = 8 columns per step), B = K
 #pragma unroll
                 for (int kk = 0; kk < kD / 32; ++kk)
-                    mma_f8_ss(s_col, sdesc_advance(q_desc, kk * 32), sdesc_advance(k_desc, kk * 32), idesc_s,
-                              kk > 0 ? 1u : 0u);
+                    mma_f8_ts(s_col, tmem + kColQ + kk * 8, sdesc_advance(k_desc, kk * 32), idesc_s, kk > 0 ? 1u : 0u);
                 mma_commit(&s_full[j & 1]);
                 mma_commit(&k_empty[ks]);
                 if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
@@ -348,7 +353,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         uint32_t s[128];
 
-        for (int j = 0; j < nkv; ++j) {
+        {
+            // copy this row of Q (128 e4m3 bytes) from the swizzled shared tile
+            // into tensor memory
+            const bool got_q = mbar_wait(q_full, 0, abort_flag, p.status, 50);
+            ok = __all_sync(0xffffffffu, got_q);
+            if (ok) {
+                uint32_t qv[32];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint4 u =
+                        *reinterpret_cast<const uint4 *>(smem + L::OFF_Q + row * 128 + ((k ^ (row & 7)) << 4));
+                    qv[k * 4 + 0] = u.x;
+                    qv[k * 4 + 1] = u.y;
+                    qv[k * 4 + 2] = u.z;
+                    qv[k * 4 + 3] = u.w;
+                }
+                tmem_st_x32(lane_base + kColQ, qv);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(q_tmem);
+            }
+        }
+
+        for (int j = 0; ok && j < nkv; ++j) {
             const int sb = j & 1;
             const bool got_s = mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.status, 47);
             if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
@@ -390,29 +418,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = mx;
                 rescale = true;
             }
-            const float bias = kLift - m_ref;
-            float l0 = 0.f, l1 = 0.f, e0 = 0.f, e1 = 0.f;
+            const float2 bias = make_float2(kLift - m_ref, kLift - m_ref);
+            const float2 sl2x2 = make_float2(sl2, sl2);
+            float2 lr01 = make_float2(0.f, 0.f), lr23 = lr01, le01 = lr01, le23 = lr01;
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, bias));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, bias));
-                const float p2 = ex2_approx(fmaf(__uint_as_float(s[c + 2]), sl2, bias));
-                const float p3 = ex2_approx(fmaf(__uint_as_float(s[c + 3]), sl2, bias));
+                const float2 x01 = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, bias);
+                const float2 x23 = ffma2(make_float2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2, bias);
+                const float p0 = ex2_approx(x01.x);
+                const float p1 = ex2_approx(x01.y);
+                const float p2 = ex2_approx(x23.x);
+                const float p3 = ex2_approx(x23.y);
                 const uint32_t w01 = cvt_e4m3x2(p0, p1);
                 const uint32_t w23 = cvt_e4m3x2(p2, p3);
                 pk[c / 4] = w01 | (w23 << 16);
-                const float2 r01 = e4m3x2_to_float2(w01);
-                const float2 r23 = e4m3x2_to_float2(w23);
-                l0 += r01.x + r01.y;
-                l1 += r23.x + r23.y;
-                e0 += p0 + p1;
-                e1 += p2 + p3;
+                lr01 = fadd2(lr01, e4m3x2_to_float2(w01));
+                lr23 = fadd2(lr23, e4m3x2_to_float2(w23));
+                le01 = fadd2(le01, make_float2(p0, p1));
+                le23 = fadd2(le23, make_float2(p2, p3));
             }
-            l_sum += l0 + l1;
-            l_exact += e0 + e1;
+            l_sum += (lr01.x + lr01.y) + (lr23.x + lr23.y);
+            l_exact += (le01.x + le01.y) + (le23.x + le23.y);
             __syncwarp();
-            tmem_st_x32(lane_base + kColP + sb * 32, pk);
+            tmem_st_x32(lane_base + kColS + sb * kBN, pk);  // P overlays the S row just read
 
             if (j >= 1) {
                 const bool got_o = mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status, 48);
