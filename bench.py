@@ -149,7 +149,11 @@ def run_ours(a):
     lib = _lib.load()
     stream = torch.cuda.current_stream()
 
-    # each rank owns its own batch shard (seeded by rank): weak scaling
+    # weak scaling: the global problem has B * ws batches; this rank owns the
+    # contiguous (batch, kv-head) units of its own B batches (no exchange)
+    from exact_attention_85_gb300.sharding import unit_range
+    u_lo, u_hi = unit_range(w.B * ws, w.Hkv, ws, rank)
+    assert u_hi - u_lo == w.B * w.Hkv
     host = make_inputs(w, seed=w.seed + 1000 * rank, with_grad=True)
     q, k, v, dO = (host[n].to(dev).contiguous() for n in ("q", "k", "v", "dO"))
     B, Hq, N, d = q.shape
@@ -243,6 +247,7 @@ def run_ours(a):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
                    "causal": w.causal, "per_gpu_batch": w.B, "global_batch": w.B * ws,
                    "parallelism": f"dp{ws} (batch shards, no collective)",
+                   "units_rank0": [u_lo, u_hi] if rank == 0 else None,
                    "l2": "flushed between steps (256 MB write); inputs 537 MB also exceed L2",
                    "backward_included": has_bwd},
         "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
