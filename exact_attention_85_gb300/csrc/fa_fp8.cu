@@ -41,6 +41,14 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
+// Two e4m3 bytes (bits 0-15) -> two fp16 values (exact), packed.
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t v) {
+    uint32_t h2;
+    const uint16_t in = (uint16_t)v;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    return h2;
+}
+
 // Two e4m3 bytes (bits 0-15) -> two floats (exact).
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v) {
     uint32_t h2;
@@ -399,14 +407,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 128; ++c)
                     if (kv0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
             }
-            float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
-            float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
+            // four chains of three-input maxima: two new scores per instruction
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int c = 4; c < 128; c += 4) {
-                mx0 = fmaxf(mx0, __uint_as_float(s[c]));
-                mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
-                mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
-                mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
+            for (int c = 0; c < 128; c += 8) {
+                mx0 = fmax3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+                mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+                mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
             }
             const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
             float alpha = 1.0f;
@@ -420,7 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float2 bias = make_float2(kLift - m_ref, kLift - m_ref);
             const float2 sl2x2 = make_float2(sl2, sl2);
-            float2 lr01 = make_float2(0.f, 0.f), lr23 = lr01, le01 = lr01, le23 = lr01;
+            float2 le01 = make_float2(0.f, 0.f), le23 = le01;
+            // the sum of the quantised P is accumulated in fp16 pairs over 32
+            // scores (at most 32 x 256: exact range, 11-bit precision) and then
+            // widened, which costs one conversion and one add per two scores
+            uint32_t hacc0 = 0u, hacc1 = 0u;
+            float lr = 0.0f;
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 128; c += 4) {
@@ -433,12 +446,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t w01 = cvt_e4m3x2(p0, p1);
                 const uint32_t w23 = cvt_e4m3x2(p2, p3);
                 pk[c / 4] = w01 | (w23 << 16);
-                lr01 = fadd2(lr01, e4m3x2_to_float2(w01));
-                lr23 = fadd2(lr23, e4m3x2_to_float2(w23));
+                hacc0 = hadd2_u32(hacc0, e4m3x2_to_h2(w01));
+                hacc1 = hadd2_u32(hacc1, e4m3x2_to_h2(w23));
+                if ((c & 31) == 28) {  // every 32 scores: widen and restart
+                    const float2 f0 = unpack2<false>(hacc0);
+                    const float2 f1 = unpack2<false>(hacc1);
+                    lr += (f0.x + f0.y) + (f1.x + f1.y);
+                    hacc0 = 0u;
+                    hacc1 = 0u;
+                }
                 le01 = fadd2(le01, make_float2(p0, p1));
                 le23 = fadd2(le23, make_float2(p2, p3));
             }
-            l_sum += (lr01.x + lr01.y) + (lr23.x + lr23.y);
+            l_sum += lr;
             l_exact += (le01.x + le01.y) + (le23.x + le23.y);
             __syncwarp();
             tmem_st_x32(lane_base + kColS + sb * kBN, pk);  // P overlays the S row just read

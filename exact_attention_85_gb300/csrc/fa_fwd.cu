@@ -291,14 +291,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 128; ++c)
                     if (kv0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
             }
-            float mx0 = __uint_as_float(s[0]), mx1 = __uint_as_float(s[1]);
-            float mx2 = __uint_as_float(s[2]), mx3 = __uint_as_float(s[3]);
+            // four chains of three-input maxima: two new scores per instruction
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int c = 4; c < 128; c += 4) {
-                mx0 = fmaxf(mx0, __uint_as_float(s[c]));
-                mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
-                mx2 = fmaxf(mx2, __uint_as_float(s[c + 2]));
-                mx3 = fmaxf(mx3, __uint_as_float(s[c + 3]));
+            for (int c = 0; c < 128; c += 8) {
+                mx0 = fmax3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+                mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+                mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
             }
             const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
             float alpha = 1.0f;
