@@ -34,18 +34,21 @@ def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None, str
 
 
 def attention_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None,
-                  workspace=None, stream=None):
-    """Returns (dQ, dK, dV) from the forward's O and LSE and the incoming dO."""
+                  workspace=None, stream=None, deterministic: bool = False):
+    """Returns (dQ, dK, dV) from the forward's O and LSE and the incoming dO.
+
+    ``deterministic=True`` forms dQ in a second pass over Q tiles instead of
+    by atomic addition (bit-identical results from run to run)."""
     import torch
     B, Hq, N, d = q.shape
     if workspace is None:
-        nbytes = _lib.fa_bwd_workspace_bytes(B, Hq, N, d)
-        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        size_fn = _lib.fa_bwd_two_pass_workspace_bytes if deterministic else _lib.fa_bwd_workspace_bytes
+        workspace = torch.empty(size_fn(B, Hq, N, d), dtype=torch.uint8, device=q.device)
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    _lib.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal, _default_scale(d) if scale is None else scale,
-                workspace, stream)
+    fn = _lib.fa_bwd_two_pass if deterministic else _lib.fa_bwd
+    fn(q, k, v, o, lse, dO, dq, dk, dv, causal, _default_scale(d) if scale is None else scale, workspace, stream)
     return dq, dk, dv
 
 

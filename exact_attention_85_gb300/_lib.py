@@ -17,7 +17,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA, FA
 FA_FP16, FA_BF16 = 0, 1
 
 EXPORTS = (
-    "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_noalloc", "fa_hadamard_quant_fp8",
+    "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_two_pass", "fa_bwd_two_pass_workspace_bytes",
+    "fa_bwd_noalloc", "fa_hadamard_quant_fp8",
     "fa_hadamard_quant_workspace_bytes", "fa_fwd_fp8", "fa_get_device_status",
     "fa_selftest_bounded_wait", "fa_status_string",
 )
@@ -45,6 +46,9 @@ def load():
         P, I, F, Z, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_long
         lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, Z, P]
+        lib.fa_bwd_two_pass.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, Z, P]
+        lib.fa_bwd_two_pass_workspace_bytes.argtypes = [I, I, I, I]
+        lib.fa_bwd_two_pass_workspace_bytes.restype = Z
         lib.fa_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
         lib.fa_bwd_workspace_bytes.restype = Z
@@ -56,7 +60,7 @@ def load():
         lib.fa_selftest_bounded_wait.argtypes = [I, P]
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_bwd", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
+        for name in ("fa_fwd", "fa_bwd", "fa_bwd_two_pass", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
                      "fa_get_device_status", "fa_selftest_bounded_wait"):
             getattr(lib, name).restype = I
         _lib = lib
@@ -112,6 +116,19 @@ def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, workspac
     _check("fa_bwd", load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
                                    _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(causal), float(scale),
                                    _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fa_bwd_two_pass_workspace_bytes(B: int, Hq: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_two_pass_workspace_bytes(B, Hq, N, d))
+
+
+def fa_bwd_two_pass(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, workspace, stream=None):
+    """Deterministic backward: dQ from a second pass over Q tiles, no atomics."""
+    B, Hq, Hkv, N, d = _dims(q, k)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fa_bwd_two_pass", load().fa_bwd_two_pass(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv,
+        N, d, int(causal), float(scale), _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, stream=None):

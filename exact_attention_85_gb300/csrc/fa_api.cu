@@ -166,7 +166,31 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, c
     float *dq_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + round256(rows * sizeof(float)));
     fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_BF16,
                   D, dq_acc};
-    return from_cuda(fa::launch_bwd(a, static_cast<cudaStream_t>(stream)));
+    return from_cuda(fa::launch_bwd(a, static_cast<cudaStream_t>(stream), false));
+}
+
+size_t fa_bwd_two_pass_workspace_bytes(int B, int Hq, int N, int d) {
+    if (B < 1 || Hq < 1 || N < 1 || d < 1) return 0;
+    return round256((size_t)B * Hq * N * sizeof(float));
+}
+
+fa_status_t fa_bwd_two_pass(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                            const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d,
+                            int causal, float scale, fa_dtype_t dtype, void *workspace, size_t workspace_bytes,
+                            void *stream) {
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
+    if (s != FA_OK) return s;
+    const size_t need = fa_bwd_two_pass_workspace_bytes(B, Hq, N, d);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FA_ERR_WORKSPACE;
+    fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_BF16,
+                  static_cast<float *>(workspace), nullptr};
+    return from_cuda(fa::launch_bwd(a, static_cast<cudaStream_t>(stream), true));
 }
 
 size_t fa_hadamard_quant_workspace_bytes(long rows, int d) {

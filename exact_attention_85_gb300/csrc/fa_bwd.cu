@@ -15,6 +15,9 @@
 //   bwd_pre_kernel   D = rowsum(dO o O) (fp32) and dQacc = 0     (HBM bound)
 //   bwd_main_kernel  the K/V-tile loop below                     (tensor bound)
 //   bwd_dq_kernel    dQ = scale * dQacc, converted to the element type
+// and, for the deterministic two-pass variant, bwd_pre_kernel (D only),
+// bwd_main_kernel without its dQ part, then bwd_dq_pass_kernel (one CTA per
+// Q tile, dQ summed on chip in a fixed order; described at the kernel).
 //
 // Main kernel, one CTA per (128-key tile, key/value head, batch); Q tiles of
 // 128 rows, so every MMA is 128 x 128 (full tensor-core rate; at 64 columns the
@@ -86,7 +89,9 @@ struct BwdParams {
 // tensor-memory columns
 constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 128, kColDV = 256, kColDK = 384;
 
-template <int D, bool BF16>
+// DQ = false builds the first pass of the deterministic two-pass backward:
+// only dK and dV, no dQ^T MMA, no dS in shared memory, no atomics.
+template <int D, bool BF16, bool DQ>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -259,11 +264,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 // dQ_i^T = K_j^T dS_i^T -> [128, 256) (lane = head-dim index);
                 // 16 keys = 16 rows = 2048 bytes of both operands per step
+                if constexpr (DQ) {
 #pragma unroll
-                for (int kk = 0; kk < kBKV / 16; ++kk)
-                    mma_f16_ss(tmem + kColDQ, sdesc_advance(kt_desc, kk * 2048), sdesc_advance(ds_desc, kk * 2048),
-                               idesc_dq, kk > 0 ? 1u : 0u);
-                mma_commit(dq_full);
+                    for (int kk = 0; kk < kBKV / 16; ++kk)
+                        mma_f16_ss(tmem + kColDQ, sdesc_advance(kt_desc, kk * 2048),
+                                   sdesc_advance(ds_desc, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
+                    mma_commit(dq_full);
+                }
                 const uint64_t qm_desc = sdesc_advance(qm_desc0, st * kStage);
                 const uint64_t dom_desc = sdesc_advance(dom_desc0, st * kStage);
                 const uint32_t acc_first = it > 0 ? 1u : 0u;
@@ -283,7 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (it + 1 < n_it) {
                     // S^T / dP^T of the next tile overwrite P^T, dS^T (read by the MMAs
                     // just issued, which run first) and dQ^T (read out once dq_free flips)
-                    if (!mbar_wait(dq_free, it & 1, abort_flag, p.status, 25)) { ok = false; break; }
+                    if constexpr (DQ) {
+                        if (!mbar_wait(dq_free, it & 1, abort_flag, p.status, 25)) { ok = false; break; }
+                    }
                     tc_fence_after();
                     if (!issue_sdp(it + 1)) { ok = false; break; }
                 }
@@ -304,6 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
         const int kv = kv0 + c;
+        // a key row past N (zero-filled by the copy) must give P = 0: its
+        // score 0 is not covered by L, and exp(0 - L) can overflow
+        const bool kv_oob = kv >= p.N;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int st = it % QS;
@@ -338,6 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (kv > q_first + r) p0 = 0.0f;
                         if (kv > q_first + r + 1) p1 = 0.0f;
                     }
+                    if (kv_oob) {
+                        p0 = 0.0f;
+                        p1 = 0.0f;
+                    }
                     const float2 t = fsub2(make_float2(__uint_as_float(dp[r]), __uint_as_float(dp[r + 1])),
                                            *reinterpret_cast<const float2 *>(dsm + r));
                     const float2 ds = fmul2(make_float2(p0, p1), t);
@@ -355,14 +371,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // reads: P^T at qc .. qc + 7, dS^T at qc + 8 .. qc + 15
                 tmem_st_x8(lane_base + kColS + qc, pp);
                 tmem_st_x8(lane_base + kColS + qc + 8, dd);
-                // dS^T row c, queries qc .. qc + 15 -> 16-byte chunks 2 ch, 2 ch + 1
-                // of the 128-byte swizzled row of box hf
+                if constexpr (DQ) {
+                    // dS^T row c, queries qc .. qc + 15 -> 16-byte chunks 2 ch, 2 ch + 1
+                    // of the 128-byte swizzled row of box hf
 #pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    *reinterpret_cast<uint4 *>(ds_row + (((2 * ch + q) ^ (c & 7)) << 4)) =
-                        make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+                    for (int q = 0; q < 2; ++q)
+                        *reinterpret_cast<uint4 *>(ds_row + (((2 * ch + q) ^ (c & 7)) << 4)) =
+                            make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+                }
             }
-            fence_proxy_async_smem();
+            if constexpr (DQ) fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(ds_ready);
@@ -416,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int t = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        for (int it = 0; it < n_it; ++it) {
+        for (int it = 0; DQ && it < n_it; ++it) {
             const bool got = mbar_wait(dq_full, it & 1, abort_flag, p.status, 29);
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
@@ -511,36 +529,372 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float4 *__restrict__ 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Second pass of the deterministic backward ([V2] section 7.2: dQ either by
+// atomic addition, as above, or by a separate pass).  The first pass is
+// bwd_main_kernel<D, BF16, false>, which produces dK and dV only.  Here every
+// CTA owns one 128-row Q tile of one query head and walks the K/V tiles of its
+// key/value head in order, so each element of dQ is accumulated by the tensor
+// core in a fixed order and stored once: the result does not depend on
+// scheduling.  Per K/V tile j, from the stored L and D:
+//   S = Q K_j^T, dP = dO V_j^T              (both operands in shared memory)
+//   P = exp2(S scale log2(e) - L log2(e)), dS = P o (dP - D)
+//   dQ += dS K_j                             (A = dS from tensor memory)
+// Tensor memory, lane = query row:
+//   [0, 128), [128, 256)  S of even / odd tiles; dS (16-bit pairs) is written
+//                          over the S columns its own warp has already read
+//   [256, 384)            dP
+//   [384, 384 + d)        dQ
+// Warps: 0-7 dS (warp w: lane quarter w % 4, keys 64 (w / 4) .. + 63), then
+// the dQ epilogue; 8 TMA producer; 9 MMA issuer + tensor-memory owner.
+constexpr int kDqThreads = 320;
+constexpr int kDqSoftmaxThreads = 256;
+constexpr int kDqProducerWarp = 8, kDqMmaWarp = 9;
+constexpr uint32_t kDqColS = 0, kDqColDP = 256, kDqColDQ = 384;
+
+template <int D>
+struct DqLayout {
+    static constexpr int NBOX = D / 64;
+    static constexpr int TILE = 128 * D * 2;  // one 128-row tile of Q, dO, K or V
+    static constexpr int BOX = 128 * 128;     // one 64-column box of a tile
+    static constexpr int KS = D == 128 ? 3 : 4;  // K is held until dQ of its tile
+    static constexpr int VS = D == 128 ? 2 : 4;  // V only until dP of its tile
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_DO = OFF_Q + TILE;
+    static constexpr int OFF_K = OFF_DO + TILE;
+    static constexpr int OFF_V = OFF_K + KS * TILE;
+    static constexpr int OFF_BAR = OFF_V + VS * TILE;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], sdp_full[2],
+    // ds_ready[2], dp_free, acc_done, drain
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 4 + 3;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int SLACK = 512;
+    static constexpr int ALLOC = BYTES + SLACK;
+    static_assert(ALLOC <= 227 * 1024, "shared memory");
+};
+
+struct DqParams {
+    const float *lse;
+    const float *Dvec;
+    unsigned int *status;
+    int Hq, Hkv, N, nq, nkv;
+    int causal;
+    float scale, scale_log2;
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kDqThreads, 1)
+    bwd_dq_pass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_dq, const DqParams p) {
+    using L = DqLayout<D>;
+    constexpr int KS = L::KS, VS = L::VS;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    if (pad > (uint32_t)L::SLACK) {  // uniform across the CTA; nothing started yet
+        if (threadIdx.x == 0) record_timeout(p.status, 0x7FFE);
+        return;
+    }
+    uint8_t *smem = smem_raw + pad;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+    uint64_t *q_full = bars;
+    uint64_t *k_full = q_full + 1;
+    uint64_t *k_empty = k_full + KS;
+    uint64_t *v_full = k_empty + KS;
+    uint64_t *v_empty = v_full + VS;
+    uint64_t *sdp_full = v_empty + VS;
+    uint64_t *ds_ready = sdp_full + 2;
+    uint64_t *dp_free = ds_ready + 2;
+    uint64_t *acc_done = dp_free + 1;
+    uint64_t *drain = acc_done + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // consecutive CTAs share a head (its K/V stay in L2); causal tiles go
+    // longest first within a head
+    const int bh = blockIdx.x / p.nq;
+    const int qt_lin = blockIdx.x - bh * p.nq;
+    const int qt = p.causal ? (p.nq - 1 - qt_lin) : qt_lin;
+    const int b = bh / p.Hq;
+    const int h = bh - b * p.Hq;
+    const int kv_plane = b * p.Hkv + h / (p.Hq / p.Hkv);
+    const int q0 = qt * 128;
+    const int n_j = p.causal ? min(qt + 1, p.nkv) : p.nkv;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < KS; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+        for (int s = 0; s < VS; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
+        for (int s = 0; s < 2; ++s) { mbar_init(&sdp_full[s], 1); mbar_init(&ds_ready[s], kDqSoftmaxThreads); }
+        mbar_init(dp_free, kDqSoftmaxThreads);
+        mbar_init(acc_done, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kDqMmaWarp) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kDqProducerWarp) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(q_full, 2 * L::TILE);
+            for (int bx = 0; bx < L::NBOX; ++bx) {
+                tma_load_3d(smem + L::OFF_Q + bx * L::BOX, &tm_q, q_full, bx * 64, q0, bh);
+                tma_load_3d(smem + L::OFF_DO + bx * L::BOX, &tm_do, q_full, bx * 64, q0, bh);
+            }
+            int nk = 0, nv = 0;  // tiles whose copies were issued
+            for (int j = 0; j < n_j; ++j) {
+                const int ks = j % KS;
+                if (j >= KS && !mbar_wait(&k_empty[ks], ((j / KS) + 1) & 1, abort_flag, p.status, 41)) break;
+                mbar_arrive_expect_tx(&k_full[ks], L::TILE);
+                for (int bx = 0; bx < L::NBOX; ++bx)
+                    tma_load_3d(smem + L::OFF_K + ks * L::TILE + bx * L::BOX, &tm_k, &k_full[ks], bx * 64,
+                                j * 128, kv_plane);
+                ++nk;
+                const int vs = j % VS;
+                if (j >= VS && !mbar_wait(&v_empty[vs], ((j / VS) + 1) & 1, abort_flag, p.status, 42)) break;
+                mbar_arrive_expect_tx(&v_full[vs], L::TILE);
+                for (int bx = 0; bx < L::NBOX; ++bx)
+                    tma_load_3d(smem + L::OFF_V + vs * L::TILE + bx * L::BOX, &tm_v, &v_full[vs], bx * 64,
+                                j * 128, kv_plane);
+                ++nv;
+            }
+            if (*abort_flag) {
+                // let copies already in flight land before the CTA exits
+                mbar_wait_drain(q_full, 0, 10000000ull);
+                for (int t = max(0, nk - KS); t < nk; ++t)
+                    mbar_wait_drain(&k_full[t % KS], (t / KS) & 1, 10000000ull);
+                for (int t = max(0, nv - VS); t < nv; ++t)
+                    mbar_wait_drain(&v_full[t % VS], (t / VS) & 1, 10000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kDqMmaWarp) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t fmt = BF16 ? 1u : 0u;
+            constexpr uint32_t idesc_sdp = make_idesc(128, 128, fmt, false, false);  // K-major both
+            constexpr uint32_t idesc_dq = make_idesc(128, D, fmt, false, true);      // A tmem, B MN-major
+            const uint64_t q_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_Q), 16, 1024);
+            const uint64_t do_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_DO), 16, 1024);
+            const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);
+            // K as the MN-major B of dQ += dS K (N = head dim, contiguous)
+            const uint64_t km_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_K), L::BOX, 1024);
+            const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_V), 16, 1024);
+
+            // dQ += dS_t K_t; 16 keys = 8 packed columns of A, 16 rows (2048
+            // bytes) of B per step.  Keys 64 h + 16 m .. + 15 of the tile have
+            // their dS at columns 64 h + 8 m .. + 7 of the S buffer.
+            auto issue_dq = [&](int t) -> bool {
+                const int sb = t & 1;
+                if (!mbar_wait(&ds_ready[sb], (t >> 1) & 1, abort_flag, p.status, 43)) return false;
+                tc_fence_after();
+                const int ks = t % KS;
+                const uint64_t km_desc = sdesc_advance(km_desc0, ks * L::TILE);
+                const uint32_t a_col = tmem + kDqColS + sb * 128;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_f16_ts(tmem + kDqColDQ, a_col + (kk >> 2) * 64 + (kk & 3) * 8,
+                               sdesc_advance(km_desc, kk * 2048), idesc_dq, (t > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&k_empty[ks]);
+                return true;
+            };
+
+            bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 44);
+            for (int j = 0; ok && j < n_j; ++j) {
+                const int ks = j % KS, vs = j % VS, sb = j & 1;
+                if (!mbar_wait(&k_full[ks], (j / KS) & 1, abort_flag, p.status, 45)) { ok = false; break; }
+                tc_fence_after();
+                // S_j into buffer sb: its previous contents, dS_{j-2}, were read
+                // by the dQ MMAs issued before (the MMAs run in issue order)
+                const uint64_t k_desc = sdesc_advance(k_desc0, ks * L::TILE);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::BOX + (kk & 3) * 32;
+                    mma_f16_ss(tmem + kDqColS + sb * 128, sdesc_advance(q_desc, off), sdesc_advance(k_desc, off),
+                               idesc_sdp, kk > 0 ? 1u : 0u);
+                }
+                // dP_j: the dS warps have loaded dP_{j-1} into registers
+                if (j > 0 && !mbar_wait(dp_free, (j - 1) & 1, abort_flag, p.status, 46)) { ok = false; break; }
+                if (!mbar_wait(&v_full[vs], (j / VS) & 1, abort_flag, p.status, 47)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t v_desc = sdesc_advance(v_desc0, vs * L::TILE);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::BOX + (kk & 3) * 32;
+                    mma_f16_ss(tmem + kDqColDP, sdesc_advance(do_desc, off), sdesc_advance(v_desc, off), idesc_sdp,
+                               kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&v_empty[vs]);
+                mma_commit(&sdp_full[sb]);
+                // dQ of the previous tile runs while the dS warps work on this one
+                if (j > 0 && !issue_dq(j - 1)) { ok = false; break; }
+            }
+            if (ok && n_j > 0) ok = issue_dq(n_j - 1);
+            if (ok) mma_commit(acc_done);
+            // every MMA issued above has completed once `drain` flips
+            mma_commit(drain);
+            mbar_wait_drain(drain, 0, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------- warps 0-7: dS, epilogue
+        const int hf = warp >> 2;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // query row == TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const int q = q0 + r;
+        const bool q_in = q < p.N;
+        // rows past N: P = 0 (their dQ rows are not stored)
+        const float nl2 = q_in ? -p.lse[(size_t)bh * p.N + q] * 1.4426950408889634f : -INFINITY;
+        const float dq_d = q_in ? p.Dvec[(size_t)bh * p.N + q] : 0.0f;
+        // last key this row attends to: causal q, and never a key past N
+        const int kv_last = p.causal ? min(q, p.N - 1) : p.N - 1;
+        const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nl2x2 = make_float2(nl2, nl2);
+        const float2 dx2 = make_float2(dq_d, dq_d);
+        bool ok = true;
+        for (int j = 0; j < n_j; ++j) {
+            const int sb = j & 1;
+            const bool got = mbar_wait(&sdp_full[sb], (j >> 1) & 1, abort_flag, p.status, 48);
+            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t dp[64];
+            tmem_ld_x32(lane_base + kDqColDP + hf * 64, dp);
+            tmem_ld_x32(lane_base + kDqColDP + hf * 64 + 32, dp + 32);
+            tmem_ld_wait_x32(dp);
+            tmem_ld_wait_x32(dp + 32);
+            tc_fence_before();
+            mbar_arrive(dp_free);
+            const int kv_first = j * 128 + hf * 64;
+            const bool masked = kv_first + 63 > kv_last;
+            const uint32_t s_cols = lane_base + kDqColS + sb * 128 + hf * 64;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t s[32];
+                tmem_ld_x32(s_cols + 32 * c, s);
+                tmem_ld_wait_x32(s);
+                uint32_t dd[16];
+#pragma unroll
+                for (int x = 0; x < 32; x += 2) {
+                    const float2 t = ffma2(make_float2(__uint_as_float(s[x]), __uint_as_float(s[x + 1])), sl2, nl2x2);
+                    float p0 = ex2_approx(t.x);
+                    float p1 = ex2_approx(t.y);
+                    if (masked) {
+                        const int kv = kv_first + 32 * c + x;
+                        if (kv > kv_last) p0 = 0.0f;
+                        if (kv + 1 > kv_last) p1 = 0.0f;
+                    }
+                    const float2 ds = fmul2(make_float2(p0, p1),
+                                            fsub2(make_float2(__uint_as_float(dp[32 * c + x]),
+                                                              __uint_as_float(dp[32 * c + x + 1])),
+                                                  dx2));
+                    dd[x / 2] = BF16 ? pack_bf16x2(ds.x, ds.y) : pack_f16x2(ds.x, ds.y);
+                }
+                __syncwarp();
+                // keys 32 c .. 32 c + 31 of this half -> packed columns 16 c .. + 15,
+                // all already read by this thread (own lane, columns < 32 (c + 1))
+                tmem_st_x16(s_cols + 16 * c, dd);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&ds_ready[sb]);
+        }
+        // ------------------------------------------------ epilogue: dQ store
+        bool ok2 = ok && mbar_wait(acc_done, 0, abort_flag, p.status, 49);
+        __syncwarp();
+        ok2 = named_bar_and(1, kDqSoftmaxThreads, ok2);
+        if (ok2) {
+            tc_fence_after();
+            // Q is no longer read once every MMA has completed: its buffer
+            // stages the output tile
+            uint8_t *stage = smem + L::OFF_Q;
+#pragma unroll 1
+            for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+                uint32_t o[32];
+                tmem_ld_x32(lane_base + kDqColDQ + c0, o);
+                tmem_ld_wait_x32(o);
+                uint32_t w[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const float a0 = __uint_as_float(o[2 * x]) * p.scale;
+                    const float a1 = __uint_as_float(o[2 * x + 1]) * p.scale;
+                    w[x] = BF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
+                }
+                uint8_t *rowp = stage + (c0 >> 6) * L::BOX + r * 128;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int chunk = ((c0 & 63) >> 3) + x;
+                    *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (r & 7)) << 4)) =
+                        make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, kDqSoftmaxThreads);
+            if (threadIdx.x == 0) {
+                for (int bx = 0; bx < L::NBOX; ++bx) tma_store_3d(&tm_dq, stage + bx * L::BOX, bx * 64, q0, bh);
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kDqMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 int elementwise_blocks() {
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     return sms * 8;
 }
 
+// two_pass = false: pre, main (with dQ atomics), dQ conversion.
+// two_pass = true:  pre (D only), main without dQ, bwd_dq_pass_kernel.
 template <int D, bool BF16>
-cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st) {
+cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
     using L = BwdLayout<D>;
     const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const uint64_t N = a.N;
     const uint64_t pq = (uint64_t)a.B * a.Hq, pkv = (uint64_t)a.B * a.Hkv;
-    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
     if (!make_tmap_3d(&tq, a.q, dt, 2, D, N, pq, 64, kBQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_3d(&tdo, a.dO, dt, 2, D, N, pq, 64, kBQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_3d(&tk, a.k, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_3d(&tv, a.v, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_3d(&tdk, a.dk, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_3d(&tdv, a.dv, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_tmap_3d(&tdv, a.dv, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        (two_pass && !make_tmap_3d(&tdq, a.dq, dt, 2, D, N, pq, 64, kBQ, CU_TENSOR_MAP_SWIZZLE_128B)))
         return cudaErrorInvalidValue;
 
     const long rows = (long)a.B * a.Hq * a.N;
     const int eb = elementwise_blocks();
     bwd_pre_kernel<BF16><<<eb, 256, 0, st>>>(static_cast<const uint4 *>(a.o), static_cast<const uint4 *>(a.dO),
                                              a.D, reinterpret_cast<float4 *>(a.dq_acc), rows, D,
-                                             rows * D / 4);
+                                             two_pass ? 0 : rows * D / 4);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    e = cudaFuncSetAttribute(bwd_main_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    auto main_kernel = two_pass ? bwd_main_kernel<D, BF16, false> : bwd_main_kernel<D, BF16, true>;
+    e = cudaFuncSetAttribute(main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     BwdParams p;
     p.lse = a.lse;
@@ -556,9 +910,32 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st) {
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     const long long grid = (long long)p.nkv * a.B * a.Hkv;
-    bwd_main_kernel<D, BF16><<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, tdo, tdk, tdv, p);
+    main_kernel<<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, tdo, tdk, tdv, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+
+    if (two_pass) {
+        using LQ = DqLayout<D>;
+        e = cudaFuncSetAttribute(bwd_dq_pass_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 LQ::ALLOC);
+        if (e != cudaSuccess) return e;
+        DqParams pq2;
+        pq2.lse = a.lse;
+        pq2.Dvec = a.D;
+        pq2.status = p.status;
+        pq2.Hq = a.Hq;
+        pq2.Hkv = a.Hkv;
+        pq2.N = a.N;
+        pq2.nq = p.nq;
+        pq2.nkv = p.nkv;
+        pq2.causal = a.causal;
+        pq2.scale = a.scale;
+        pq2.scale_log2 = p.scale_log2;
+        const long long grid2 = (long long)p.nq * a.B * a.Hq;
+        bwd_dq_pass_kernel<D, BF16><<<dim3((unsigned)grid2), dim3(kDqThreads), LQ::ALLOC, st>>>(tq, tk, tv, tdo,
+                                                                                                 tdq, pq2);
+        return cudaGetLastError();
+    }
 
     bwd_dq_kernel<BF16><<<eb, 256, 0, st>>>(reinterpret_cast<const float4 *>(a.dq_acc),
                                             static_cast<uint4 *>(a.dq), rows * D / 8, a.scale);
@@ -567,9 +944,9 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st) {
-    if (a.d == 128) return a.bf16 ? launch_bwd_t<128, true>(a, st) : launch_bwd_t<128, false>(a, st);
-    if (a.d == 64) return a.bf16 ? launch_bwd_t<64, true>(a, st) : launch_bwd_t<64, false>(a, st);
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool two_pass) {
+    if (a.d == 128) return a.bf16 ? launch_bwd_t<128, true>(a, st, two_pass) : launch_bwd_t<128, false>(a, st, two_pass);
+    if (a.d == 64) return a.bf16 ? launch_bwd_t<64, true>(a, st, two_pass) : launch_bwd_t<64, false>(a, st, two_pass);
     return cudaErrorInvalidValue;
 }
 

@@ -36,7 +36,7 @@ struct BwdArgs {
     float scale;
     bool bf16;
     float *D;      // [B][Hq][N]
-    float *dq_acc; // [B][Hq][N][d]
+    float *dq_acc; // [B][Hq][N][d]; unused (may be null) by the two-pass backward
 };
 
 struct Fp8FwdArgs {
@@ -59,7 +59,7 @@ struct QuantArgs {
 };
 
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st);
-cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st);
+cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool two_pass);
 cudaError_t launch_fwd_fp8(const Fp8FwdArgs &a, cudaStream_t st);
 cudaError_t launch_hadamard_quant(const QuantArgs &a, cudaStream_t st);
 cudaError_t launch_selftest_wait(int timeout_us, cudaStream_t st);

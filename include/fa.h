@@ -96,6 +96,34 @@ fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o,
                    size_t workspace_bytes, void *stream);
 
 /*
+ * Bytes of device workspace fa_bwd_two_pass needs: D only (B*Hq*N fp32,
+ * rounded up to 256 bytes).
+ */
+size_t fa_bwd_two_pass_workspace_bytes(int B, int Hq, int N, int d);
+
+/*
+ * Deterministic backward: the same results as fa_bwd, but dQ is formed by a
+ * second pass instead of atomic addition, so repeated calls on the same
+ * inputs give bit-identical dQ, dK and dV.
+ * [V2] section 7.2 (dQ is combined across K/V column blocks either by atomic
+ * addition or in two passes).  Pass 1 walks K/V column blocks as fa_bwd does
+ * and produces dK and dV only.  Pass 2 walks Q row blocks: for Q tile i it
+ * recomputes S = Q_i K_j^T, P = exp(S - L_i) and dS = P o (dP - D_i) for
+ * every K/V tile j in order and forms dQ_i = scale * sum_j dS K_j on chip,
+ * stored once.  S and dP are computed twice in total (once per pass).
+ *   Arguments, layouts and results: as fa_bwd.
+ *   workspace: device buffer of at least
+ *   fa_bwd_two_pass_workspace_bytes(B,Hq,N,d) bytes, 256-byte aligned; its
+ *   contents on entry do not matter.
+ */
+fa_status_t fa_bwd_two_pass(const void *q, const void *k, const void *v,
+                            const void *o, const float *lse, const void *dO,
+                            void *dq, void *dk, void *dv, int B, int Hq,
+                            int Hkv, int N, int d, int causal, float scale,
+                            fa_dtype_t dtype, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/*
  * Size of the scratch buffer built into the library for fa_bwd_noalloc:
  * 64 MiB per device.
  */

@@ -1,0 +1,129 @@
+"""Deterministic two-pass backward (fa_bwd_two_pass) against the fp64
+oracle, plus its run-to-run bit identity and its agreement with fa_bwd.
+Tolerance: relative Frobenius error <= 1e-2 per tensor (as for fa_bwd)."""
+import pytest
+import torch
+
+import oracle
+from exact_attention_85_gb300 import _lib
+from exact_attention_85_gb300.inputs import HEADLINE, WORKLOADS, make_custom, make_inputs
+
+from _tol import check_grad
+
+pytestmark = pytest.mark.gpu
+
+
+def _fwd(x, causal, scale):
+    q, k, v, dO = (x[n].cuda().contiguous() for n in ("q", "k", "v", "dO"))
+    B, Hq, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+    _lib.fa_fwd(q, k, v, o, lse, causal, scale)
+    return q, k, v, dO, o, lse
+
+
+def _two_pass(t, causal, scale):
+    q, k, v, dO, o, lse = t
+    B, Hq, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(_lib.fa_bwd_two_pass_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device="cuda")
+    ws.fill_(0xFF)  # contents on entry must not matter
+    _lib.fa_bwd_two_pass(q, k, v, o, lse, dO, dq, dk, dv, causal, scale, ws)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    return dq, dk, dv
+
+
+def _atomic(t, causal, scale):
+    q, k, v, dO, o, lse = t
+    B, Hq, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(_lib.fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device="cuda")
+    _lib.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal, scale, ws)
+    torch.cuda.synchronize()
+    return dq, dk, dv
+
+
+SHAPES = [
+    # B, Hq, Hkv, N, d, dtype, causal
+    (1, 1, 1, 1, 128, torch.bfloat16, True),
+    (1, 1, 1, 1, 64, torch.float16, False),
+    (1, 2, 2, 64, 128, torch.bfloat16, True),
+    (1, 2, 1, 127, 128, torch.bfloat16, False),
+    (1, 2, 2, 129, 64, torch.float16, True),
+    (2, 4, 2, 300, 128, torch.bfloat16, True),
+    (2, 4, 4, 300, 64, torch.bfloat16, False),
+    (1, 4, 1, 500, 128, torch.bfloat16, True),
+    (1, 6, 2, 384, 64, torch.float16, True),
+    (2, 2, 2, 640, 128, torch.float16, False),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,dtype,causal", SHAPES)
+def test_two_pass_small_full_compare(cuda_lib, B, Hq, Hkv, N, d, dtype, causal):
+    x = make_custom(B, Hq, Hkv, N, d, dtype, seed=N * 7 + d + Hq)
+    scale = d ** -0.5
+    dq, dk, dv = _two_pass(_fwd(x, causal, scale), causal, scale)
+    rq, rk, rv = oracle.attention_bwd(x["q"], x["k"], x["v"], x["dO"], causal, scale)
+    check_grad(dq, rq, "dQ")
+    check_grad(dk, rk, "dK")
+    check_grad(dv, rv, "dV")
+
+
+def test_two_pass_bit_identical_runs_and_matches_atomic_path(cuda_lib):
+    """Every output element is produced by one fixed sequence of operations:
+    two runs agree bit for bit.  dK and dV come from the same first-pass
+    arithmetic as fa_bwd (bit-identical to it); dQ differs from fa_bwd's
+    only by the order of the fp32 additions."""
+    x = make_custom(2, 4, 2, 700, 128, torch.bfloat16, seed=5)
+    t = _fwd(x, True, 0.09)
+    a = _two_pass(t, True, 0.09)
+    b = _two_pass(t, True, 0.09)
+    for u, w in zip(a, b):
+        assert torch.equal(u, w)
+    c = _atomic(t, True, 0.09)
+    assert torch.equal(a[1], c[1]) and torch.equal(a[2], c[2])
+    rel = float((a[0].float() - c[0].float()).norm() / c[0].float().norm())
+    assert rel < 1e-3
+
+
+@pytest.mark.parametrize("two_pass", [False, True])
+def test_ragged_tail_with_very_negative_scores(cuda_lib, two_pass):
+    """Every real score of a row near -200 (so L is near -200) and N not a
+    multiple of the tile: the zero-filled key rows past N would give
+    exp(0 - L) = inf if they were not masked."""
+    B, H, N, d = 1, 2, 200, 64
+    g = torch.Generator().manual_seed(11)
+    base = torch.full((B, H, N, d), 5.0)
+    q = (base + 0.05 * torch.randn(B, H, N, d, generator=g)).to(torch.bfloat16)
+    k = (-base + 0.05 * torch.randn(B, H, N, d, generator=g)).to(torch.bfloat16)
+    v = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16)
+    dO = torch.randn(B, H, N, d, generator=g).to(torch.bfloat16)
+    x = {"q": q, "k": k, "v": v, "dO": dO}
+    scale = 0.125
+    t = _fwd(x, False, scale)
+    assert float(t[5].max()) < -150.0
+    dq, dk, dv = (_two_pass if two_pass else _atomic)(t, False, scale)
+    for u in (dq, dk, dv):
+        assert torch.isfinite(u).all()
+    rq, rk, rv = oracle.attention_bwd(q, k, v, dO, False, scale)
+    check_grad(dq, rq, "dQ")
+    check_grad(dk, rk, "dK")
+    check_grad(dv, rv, "dV")
+
+
+@pytest.mark.parametrize("name", ["gqa_bf16_b4_hq32_hkv8_n4k_causal", HEADLINE])
+def test_two_pass_full_size_sampled_group(cuda_lib, name):
+    """Full-size launch; the oracle checks one (batch, kv-head) group entirely
+    and the rest is checked for finiteness."""
+    w = WORKLOADS[name]
+    x = make_inputs(w)
+    dq, dk, dv = _two_pass(_fwd(x, w.causal, w.scale), w.causal, w.scale)
+    b, g = w.B - 1, w.Hkv - 1
+    G = w.Hq // w.Hkv
+    rq, rk, rv = oracle.attention_bwd_group(x["q"], x["k"], x["v"], x["dO"], b, g, w.causal, w.scale)
+    check_grad(dq[b, g * G:(g + 1) * G], rq, f"{name} dQ")
+    check_grad(dk[b, g], rk, f"{name} dK")
+    check_grad(dv[b, g], rv, f"{name} dV")
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
