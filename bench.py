@@ -40,6 +40,7 @@ def _args():
     ap.add_argument("--workload", default=None, help="workload name (default: the headline shape)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-two-pass", action="store_true", help="skip the deterministic two-pass backward leg")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 leg (outlier workload)")
     return ap.parse_args()
 
@@ -258,6 +259,9 @@ def run_ours(a):
         "clocks": clk.summary(),
     }
 
+    if has_bwd and not a.no_two_pass:
+        result["two_pass_bwd_leg"] = _two_pass_leg(a, w, (q, k, v, o, lse, dO, dq, dk, dv), dev, stream, peaks,
+                                                   flush)
     if not a.no_fp8 and a.workload is None:
         result["fp8_leg"] = _fp8_leg(a, dev, stream, peaks)
     if not a.no_e2e:
@@ -268,6 +272,43 @@ def run_ours(a):
         print(json.dumps(result), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def _two_pass_leg(a, w, t, dev, stream, peaks, flush):
+    """The deterministic two-pass backward (fa_bwd_two_pass) on the step's
+    workload, timed like the step's backward.  TFLOPS count the same five
+    matrix products as fa_bwd; the two-pass form executes seven (S and dP are
+    formed once in each pass)."""
+    import torch
+
+    from exact_attention_85_gb300 import _lib
+
+    q, k, v, o, lse, dO, dq, dk, dv = t
+    B, Hq, N, d = q.shape
+    ws = torch.empty(_lib.fa_bwd_two_pass_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device=dev)
+
+    def bwd():
+        _lib.fa_bwd_two_pass(q, k, v, o, lse, dO, dq, dk, dv, w.causal, w.scale, ws, stream)
+
+    for _ in range(max(3, a.warmup)):
+        bwd()
+        flush.zero_()
+    torch.cuda.synchronize()
+    steps = max(3, min(a.steps, 10))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        bwd()
+        ev[i][1].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if _lib.fa_get_device_status(stream) != _lib.FA_OK:
+        raise RuntimeError("a bounded device wait ran out during the two-pass backward leg")
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    tf = w.bwd_flops() / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "bwd_ms": round(ms, 4), "bwd_tflops": round(tf, 1),
+            "bwd_frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+            "executed_tflops": round(tf * 7.0 / 5.0, 1), "launches_per_step": 3, "deterministic": True}
 
 
 def _fp8_leg(a, dev, stream, peaks):
