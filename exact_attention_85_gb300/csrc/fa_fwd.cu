@@ -1,32 +1,32 @@
 // fa_fwd.cu -- FlashAttention-2 forward for sm_103a (bf16 / fp16, d = 64, 128).
 //
 // Algorithm ("6.2 FlashAttention V2 chi tiet", section 6.1; blog.csdn.net
-// FlashAttention-2 article, 3.1.1): one CTA per (Q tile of 128 rows, query
-// head, batch); the Q tile is loaded once and stays in shared memory while the
-// CTA walks the K/V tiles; the running row max m and row sum l are updated per
-// tile, the output is accumulated unnormalised and divided by l once at the
-// end, and only L = m + log l is stored.  Causal: tiles above the diagonal are
-// never visited (the loop stops at the diagonal tile) and only the diagonal
-// tile is masked element-wise (section 5.3).
+// FlashAttention-2 article, 3.1.1): every 128-row Q tile is loaded once and
+// stays on chip while the K/V tiles stream past; the running row max m and
+// row sum l are updated per tile, the output is accumulated unnormalised and
+// divided by l once at the end, and only L = m + log l is stored.  Causal:
+// tiles above the diagonal are never visited (the loop stops at the diagonal
+// tile) and only the diagonal tile is masked element-wise (section 5.3).
 //
-// GB300 realisation (warp-specialised, one CTA per SM):
-//   warp 4  lane 0   TMA producer for Q (once) and the K ring
-//   warp 6  lane 0   TMA producer for the V ring
-//   warp 5  lane 0   tcgen05 MMA issuer; warp 5 also owns the TMEM allocation
-//   warps 0-3        softmax: thread t owns query row t = TMEM lane t, so a
-//                    row's max and sum never leave one thread (the page's
-//                    split of rows across warps, section 4.2, taken to its
-//                    limit), then the epilogue.
+// GB300 realisation: one CTA per SM owns TWO Q tiles (A = rows 0-127,
+// B = rows 128-255 of a 256-row block) of one (head, batch), and both walk the
+// same K/V stream, so each K/V tile is read once for 256 query rows.  The two
+// tiles' softmax warpgroups take turns on the tensor cores: while one
+// warpgroup turns S into P, the tensor cores run the other tile's
+// P.V and next S (the Blackwell form of the ping-pong the FA3 summary
+// describes for two warpgroups).
+//   warps 0-3  softmax + epilogue of tile A (thread = query row = TMEM lane)
+//   warps 4-7  softmax + epilogue of tile B
+//   warp 8     TMA producer (Q once, K ring, V ring)
+//   warp 9     tcgen05 MMA issuer; owns the TMEM allocation
 // Tensor memory (512 columns x 128 lanes, fp32):
-//   [0,128) S buffer 0   [128,256) S buffer 1   [256,256+d) O accumulator
-//   [384,384+d/2) Q (16-bit pairs, the A operand of S = Q K^T, copied once)
-// P (16-bit pairs) overwrites the first 64 columns of its own S buffer (each
-// softmax thread writes only its own lane, after reading the whole row) and is
-// the A operand of the P.V MMA.  With Q and P read from tensor memory only K
-// and V occupy the shared-memory operand path (128 bytes / cycle).
-// Pipeline per K/V tile j: MMA S_j = Q K_j^T -> softmax_j (P_j, row stats)
-// -> MMA O += P_j V_j.  S is double-buffered so S_{j+1} runs on the tensor
-// cores while softmax_j runs, and softmax_{j+1} overlaps O += P_j V_j.
+//   [0,128) S_A   [128,256) S_B   [256,256+d) O_A   [384,384+d) O_B
+// P (16-bit pairs) overwrites the first 64 columns of its own S (each softmax
+// thread writes only its own lane, after reading the whole row) and is the A
+// operand of the P.V MMA.  MMA order per K/V tile j:
+//   O_A += P_A(j) V_j,  S_A(j+1) = Q_A K_{j+1}^T,  O_B += P_B(j) V_j,  S_B(j+1)
+// so S_X(j+1) completes only after O_X += P_X(j) V_j, and a softmax thread
+// that needs to rescale O_X may do so as soon as it has seen S_X(j+1).
 //
 // Exact lazy rescaling: the reference max m_ref of a row moves only when the
 // tile max exceeds it by more than 8 (log2 units); then O and l are rescaled
@@ -40,38 +40,40 @@ namespace fa {
 
 namespace {
 
-constexpr int kBM = 128;      // query rows per CTA (TMEM lanes)
-constexpr int kBN = 128;      // keys per K/V tile
-constexpr int kThreads = 224; // 7 warps
+constexpr int kBM = 128;       // query rows per Q tile (TMEM lanes)
+constexpr int kBN = 128;       // keys per K/V tile
+constexpr int kThreads = 320;  // 10 warps
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;
 
 template <int D>
 struct FwdLayout {
-    static constexpr int KS = 3;  // K ring depth
-    static constexpr int VS = 2;  // V ring depth
-    static constexpr int NBOX = D / 64;           // 64-column (128-byte) boxes
-    static constexpr int TILE_Q = kBM * D * 2;    // bytes
-    static constexpr int TILE_KV = kBN * D * 2;
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + TILE_Q;
-    static constexpr int OFF_V = OFF_K + KS * TILE_KV;
-    static constexpr int OFF_BAR = OFF_V + VS * TILE_KV;
-    // q_full, q_tmem, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS],
-    // s_full[2], p_full[2], o_done, drain
-    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 2 + 1 + 1;
+    static constexpr int KS = D == 128 ? 3 : 4;  // K ring depth
+    static constexpr int VS = D == 128 ? 2 : 4;  // V ring depth
+    static constexpr int NBOX = D / 64;          // 64-column (128-byte) boxes
+    static constexpr int TILE = 128 * D * 2;     // one 128-row tile, bytes
+    static constexpr int BOX = 128 * 128;        // one 64-column box of a tile
+    static constexpr int OFF_Q = 0;              // Q_A, then Q_B
+    static constexpr int OFF_K = OFF_Q + 2 * TILE;
+    static constexpr int OFF_V = OFF_K + KS * TILE;
+    static constexpr int OFF_BAR = OFF_V + VS * TILE;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
+    // p_full[2], o_final[2], drain
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 + 2 + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
+    static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
 struct FwdParams {
     float *lse;
     unsigned int *status;
-    int Hq, Hkv, N, nqt, causal;
-    float scale_log2;  // scale * log2(e)
+    int Hq, Hkv, N, nblk, causal;  // nblk: 256-row blocks per head
+    float scale_log2;              // scale * log2(e)
 };
 
-constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;
+constexpr uint32_t kColS = 0, kColO = 256;  // + 128 per tile
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -83,47 +85,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *q_full = bars;
-    uint64_t *q_tmem = bars + 1;
-    uint64_t *k_full = q_tmem + 1;
+    uint64_t *k_full = q_full + 1;
     uint64_t *k_empty = k_full + L::KS;
     uint64_t *v_full = k_empty + L::KS;
     uint64_t *v_empty = v_full + L::VS;
-    uint64_t *s_full = v_empty + L::VS;
-    uint64_t *p_full = s_full + 2;
-    uint64_t *o_done = p_full + 2;
-    uint64_t *drain = o_done + 1;
+    uint64_t *s_full = v_empty + L::VS;  // [2], one per tile
+    uint64_t *p_full = s_full + 2;       // [2]
+    uint64_t *o_final = p_full + 2;      // [2]
+    uint64_t *drain = o_final + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Tile schedule: consecutive CTAs share a head (K/V stay hot in L2);
-    // within a head, causal tiles go longest first.
-    const int bh = blockIdx.x / p.nqt;
-    const int qt_lin = blockIdx.x - bh * p.nqt;
-    const int qt = p.causal ? (p.nqt - 1 - qt_lin) : qt_lin;
+    // Block schedule: consecutive CTAs share a head (K/V stay hot in L2);
+    // within a head, causal blocks go longest first.
+    const int bh = blockIdx.x / p.nblk;
+    const int t_lin = blockIdx.x - bh * p.nblk;
+    const int t = p.causal ? (p.nblk - 1 - t_lin) : t_lin;
     const int b = bh / p.Hq;
     const int h = bh - b * p.Hq;
     const int hk = h / (p.Hq / p.Hkv);
-    const int q0 = qt * kBM;
+    const int q0a = t * 2 * kBM;
     const int nkv_all = (p.N + kBN - 1) / kBN;
-    const int nkv = p.causal ? min(qt + 1, nkv_all) : nkv_all;
+    // K/V tiles each Q tile visits; 0 for a tile that lies entirely past N
+    const int nA = p.causal ? min(q0a / kBN + 1, nkv_all) : nkv_all;
+    const int nB = q0a + kBM >= p.N ? 0 : (p.causal ? min((q0a + kBM) / kBN + 1, nkv_all) : nkv_all);
+    const int nmax = max(nA, nB);
     const int kv_plane = b * p.Hkv + hk;
     const int q_plane = b * p.Hq + h;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(q_tmem, kBM);
         for (int s = 0; s < L::KS; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
         for (int s = 0; s < L::VS; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
-        for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&p_full[s], kBM); }
-        mbar_init(o_done, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], kBM);
+            mbar_init(&o_final[x], 1);
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -132,99 +138,118 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
-        // ---------------------------------------------------- Q + K producer
+    if (warp == kProducerWarp) {
+        // -------------------------------------------------------- TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
-            mbar_arrive_expect_tx(q_full, L::TILE_Q);
-            for (int bx = 0; bx < L::NBOX; ++bx)
-                tma_load_3d(smem + L::OFF_Q + bx * kBM * 128, &tm_q, q_full, bx * 64, q0, q_plane);
-            int j = 0;
-            for (; j < nkv; ++j) {
-                const int s = j % L::KS;
-                if (j >= L::KS && !mbar_wait(&k_empty[s], ((j / L::KS) + 1) & 1, abort_flag, p.status, 1)) break;
-                mbar_arrive_expect_tx(&k_full[s], L::TILE_KV);
-                uint8_t *dst = smem + L::OFF_K + s * L::TILE_KV;
+            prefetch_tmap(&tm_v);
+            const int ntq = nB > 0 ? 2 : 1;
+            mbar_arrive_expect_tx(q_full, ntq * L::TILE);
+            for (int x = 0; x < ntq; ++x)
                 for (int bx = 0; bx < L::NBOX; ++bx)
-                    tma_load_3d(dst + bx * kBN * 128, &tm_k, &k_full[s], bx * 64, j * kBN, kv_plane);
+                    tma_load_3d(smem + L::OFF_Q + x * L::TILE + bx * L::BOX, &tm_q, q_full, bx * 64, q0a + x * kBM,
+                                q_plane);
+            // K_j then V_j: the order in which the MMAs first need them
+            int nk = 0, nv = 0;
+            for (int j = 0; j < nmax; ++j) {
+                const int ks = j % L::KS;
+                if (j >= L::KS && !mbar_wait(&k_empty[ks], ((j / L::KS) + 1) & 1, abort_flag, p.status, 1)) break;
+                mbar_arrive_expect_tx(&k_full[ks], L::TILE);
+                for (int bx = 0; bx < L::NBOX; ++bx)
+                    tma_load_3d(smem + L::OFF_K + ks * L::TILE + bx * L::BOX, &tm_k, &k_full[ks], bx * 64, j * kBN,
+                                kv_plane);
+                ++nk;
+                const int vs = j % L::VS;
+                if (j >= L::VS && !mbar_wait(&v_empty[vs], ((j / L::VS) + 1) & 1, abort_flag, p.status, 2)) break;
+                mbar_arrive_expect_tx(&v_full[vs], L::TILE);
+                for (int bx = 0; bx < L::NBOX; ++bx)
+                    tma_load_3d(smem + L::OFF_V + vs * L::TILE + bx * L::BOX, &tm_v, &v_full[vs], bx * 64, j * kBN,
+                                kv_plane);
+                ++nv;
             }
             if (*abort_flag) {
                 // let copies already in flight land before the CTA exits
-                for (int t = max(0, j - L::KS); t < j; ++t)
-                    mbar_wait_drain(&k_full[t % L::KS], (t / L::KS) & 1, 10000000ull);
                 mbar_wait_drain(q_full, 0, 10000000ull);
+                for (int u = max(0, nk - L::KS); u < nk; ++u)
+                    mbar_wait_drain(&k_full[u % L::KS], (u / L::KS) & 1, 10000000ull);
+                for (int u = max(0, nv - L::VS); u < nv; ++u)
+                    mbar_wait_drain(&v_full[u % L::VS], (u / L::VS) & 1, 10000000ull);
             }
         }
         __syncwarp();
-    } else if (warp == 6) {
-        // -------------------------------------------------------- V producer
-        if (lane == 0) {
-            prefetch_tmap(&tm_v);
-            int j = 0;
-            for (; j < nkv; ++j) {
-                const int s = j % L::VS;
-                if (j >= L::VS && !mbar_wait(&v_empty[s], ((j / L::VS) + 1) & 1, abort_flag, p.status, 2)) break;
-                mbar_arrive_expect_tx(&v_full[s], L::TILE_KV);
-                uint8_t *dst = smem + L::OFF_V + s * L::TILE_KV;
-                for (int bx = 0; bx < L::NBOX; ++bx)
-                    tma_load_3d(dst + bx * kBN * 128, &tm_v, &v_full[s], bx * 64, j * kBN, kv_plane);
-            }
-            if (*abort_flag) {
-                for (int t = max(0, j - L::VS); t < j; ++t)
-                    mbar_wait_drain(&v_full[t % L::VS], (t / L::VS) & 1, 10000000ull);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t fmt = BF16 ? 1u : 0u;
-            constexpr uint32_t idesc_s = make_idesc(kBM, kBN, fmt, false, false);
-            constexpr uint32_t idesc_pv = make_idesc(kBM, D, fmt, false, true);
+            constexpr uint32_t idesc_s = make_idesc(kBM, kBN, fmt, false, false);  // K-major both
+            constexpr uint32_t idesc_pv = make_idesc(kBM, D, fmt, false, true);    // A tmem, B MN-major
             // one descriptor per operand tile; steps are derived by sdesc_advance
+            const uint64_t q_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_Q), 16, 1024);
             const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);
-            const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_V), kBN * 128, 1024);
-            // Q is in tensor memory once the softmax warps have copied it
-            bool ok = mbar_wait(q_tmem, 0, abort_flag, p.status, 3);
-            tc_fence_after();
+            const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_V), L::BOX, 1024);
+            int k_ready = -1;  // highest K tile whose arrival has been observed
 
-            auto issue_pv = [&](int t) -> bool {
-                const int pb = t & 1;
-                if (!mbar_wait(&p_full[pb], (t >> 1) & 1, abort_flag, p.status, 4)) return false;
-                const int vs = t % L::VS;
-                if (!mbar_wait(&v_full[vs], (t / L::VS) & 1, abort_flag, p.status, 5)) return false;
+            auto wait_k = [&](int j) -> bool {
+                if (j <= k_ready) return true;
+                if (!mbar_wait(&k_full[j % L::KS], (j / L::KS) & 1, abort_flag, p.status, 3)) return false;
                 tc_fence_after();
-                const uint64_t v_desc = sdesc_advance(v_desc0, vs * L::TILE_KV);
-                const uint32_t p_col = tmem + kColS + pb * kBN;  // P overlays its S buffer
-                // B = V (N = d contiguous: MN-major); 16 keys = 16 rows of 128 B
-                mma_f16_ts(tmem + kColO, p_col, v_desc, idesc_pv, t > 0 ? 1u : 0u);
+                k_ready = j;
+                return true;
+            };
+            // S_x(j) = Q_x K_j^T (A = Q, B = K, both K-major, 32 bytes per step
+            // inside a 128-byte row)
+            auto issue_s = [&](int x, int j) {
+                const uint64_t q_desc = sdesc_advance(q_desc0, x * L::TILE);
+                const uint64_t k_desc = sdesc_advance(k_desc0, (j % L::KS) * L::TILE);
 #pragma unroll
-                for (int kk = 1; kk < kBN / 16; ++kk)
-                    mma_f16_ts(tmem + kColO, p_col + kk * 8, sdesc_advance(v_desc, kk * 16 * 128), idesc_pv, 1u);
-                mma_commit(o_done);
-                mma_commit(&v_empty[vs]);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * L::BOX + (kk & 3) * 32;
+                    mma_f16_ss(tmem + kColS + x * 128, sdesc_advance(q_desc, off), sdesc_advance(k_desc, off), idesc_s,
+                               kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&s_full[x]);
+            };
+            // O_x += P_x(j) V_j (A = P from tensor memory, 16 keys = 8 columns
+            // per step; B = V, MN-major, 16 rows of 128 bytes per step)
+            auto issue_pv = [&](int x, int j) -> bool {
+                if (!mbar_wait(&p_full[x], j & 1, abort_flag, p.status, 4)) return false;
+                tc_fence_after();
+                const uint64_t v_desc = sdesc_advance(v_desc0, (j % L::VS) * L::TILE);
+                const uint32_t p_col = tmem + kColS + x * 128;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_f16_ts(tmem + kColO + x * 128, p_col + kk * 8, sdesc_advance(v_desc, kk * 2048), idesc_pv,
+                               (j > 0 || kk > 0) ? 1u : 0u);
                 return true;
             };
 
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int ks = j % L::KS;
-                if (!mbar_wait(&k_full[ks], (j / L::KS) & 1, abort_flag, p.status, 6)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t k_desc = sdesc_advance(k_desc0, ks * L::TILE_KV);
-                const uint32_t s_col = tmem + kColS + (j & 1) * kBN;
-                // A = Q from tensor memory (16 head-dim values = 8 columns per
-                // step), B = K (K-major, 32 bytes per step inside a 128-byte row)
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * (kBN * 128) + (kk & 3) * 32;
-                    mma_f16_ts(s_col, tmem + kColQ + kk * 8, sdesc_advance(k_desc, off), idesc_s, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&s_full[j & 1]);
-                mma_commit(&k_empty[ks]);
-                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+            bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 5);
+            if (ok) ok = wait_k(0);
+            if (ok) {
+                issue_s(0, 0);
+                if (nB > 0) issue_s(1, 0);
+                mma_commit(&k_empty[0]);
             }
-            if (ok && nkv > 0) issue_pv(nkv - 1);
+            for (int j = 0; ok && j < nmax; ++j) {
+                if (!mbar_wait(&v_full[j % L::VS], (j / L::VS) & 1, abort_flag, p.status, 6)) { ok = false; break; }
+                tc_fence_after();
+                for (int x = 0; x < 2; ++x) {
+                    const int nx = x ? nB : nA;
+                    if (j >= nx) continue;
+                    if (!issue_pv(x, j)) { ok = false; break; }
+                    if (j + 1 < nx) {
+                        // S_x(j+1) overwrites P_x(j), which the MMAs just issued read first
+                        if (!wait_k(j + 1)) { ok = false; break; }
+                        issue_s(x, j + 1);
+                    } else {
+                        mma_commit(&o_final[x]);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&v_empty[j % L::VS]);
+                if (j + 1 < nmax) mma_commit(&k_empty[(j + 1) % L::KS]);
+            }
             // every MMA issued above has completed once `drain` flips
             mma_commit(drain);
             mbar_wait_drain(drain, 0, 100000000ull);
@@ -232,48 +257,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ softmax + epilogue
-        const int row = threadIdx.x;  // 0..127 == TMEM lane
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int x = warp >> 2;  // tile
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // query row within the tile == TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t col_s = kColS + x * 128, col_o = kColO + x * 128;
+        const int q0 = q0a + x * kBM;
+        const int nx = x ? nB : nA;
         const float sl2 = p.scale_log2;
         float m_ref = -INFINITY;
         float l_sum = 0.0f;    // sum of the rounded P fed to the MMA: normalises O
         float l_exact = 0.0f;  // sum of the unrounded P: gives L
         bool ok = true;
-        uint32_t s[128];
 
-        {
-            // copy this row of Q from the swizzled shared tile into tensor memory
-            const bool got_q = mbar_wait(q_full, 0, abort_flag, p.status, 10);
-            ok = __all_sync(0xffffffffu, got_q);
-            if (ok) {
-                uint32_t qv[D / 2];
-#pragma unroll
-                for (int bx = 0; bx < L::NBOX; ++bx)
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(smem + L::OFF_Q + bx * kBM * 128 + row * 128 +
-                                                                         ((k ^ (row & 7)) << 4));
-                        qv[bx * 32 + k * 4 + 0] = u.x;
-                        qv[bx * 32 + k * 4 + 1] = u.y;
-                        qv[bx * 32 + k * 4 + 2] = u.z;
-                        qv[bx * 32 + k * 4 + 3] = u.w;
-                    }
-#pragma unroll
-                for (int c0 = 0; c0 < D / 2; c0 += 32) tmem_st_x32(lane_base + kColQ + c0, qv + c0);
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(q_tmem);
-            }
-        }
-
-        for (int j = 0; ok && j < nkv; ++j) {
-            const int sb = j & 1;
+        for (int j = 0; ok && j < nx; ++j) {
             // every lane waits, then the warp votes: the tcgen05.ld/st below
             // are warp-collective (.sync.aligned) and need all 32 lanes
-            const bool got_s = mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.status, 7);
+            const bool got_s = mbar_wait(&s_full[x], j & 1, abort_flag, p.status, 7);
             if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t s_addr = lane_base + kColS + sb * kBN;
+            uint32_t s[128];
+            const uint32_t s_addr = lane_base + col_s;
             tmem_ld_x32(s_addr + 0, s + 0);
             tmem_ld_x32(s_addr + 32, s + 32);
             tmem_ld_x32(s_addr + 64, s + 64);
@@ -310,112 +314,112 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = mx;
                 rescale = true;
             }
+            __syncwarp();  // reconverge after the per-row branches above
             const float2 neg_m = make_float2(-m_ref, -m_ref);
             const float2 sl2x2 = make_float2(sl2, sl2);
             float2 lr01 = make_float2(0.f, 0.f), lr23 = lr01, le01 = lr01, le23 = lr01;
-            uint32_t pk[64];
 #pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                const float2 x01 = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, neg_m);
-                const float2 x23 =
-                    ffma2(make_float2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2, neg_m);
-                const float p0 = ex2_approx(x01.x);
-                const float p1 = ex2_approx(x01.y);
-                const float p2 = ex2_approx(x23.x);
-                const float p3 = ex2_approx(x23.y);
-                // l sums the rounded P that the MMA consumes, so O~ / l is an
-                // exactly normalised mix of V rows even when one term dominates
-                if constexpr (BF16) {
-                    pk[c / 2] = pack_bf16x2(p0, p1);
-                    pk[c / 2 + 1] = pack_bf16x2(p2, p3);
-                } else {
-                    pk[c / 2] = pack_f16x2(p0, p1);
-                    pk[c / 2 + 1] = pack_f16x2(p2, p3);
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 64 * hh; c < 64 * hh + 64; c += 4) {
+                    const float2 x01 =
+                        ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, neg_m);
+                    const float2 x23 =
+                        ffma2(make_float2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2, neg_m);
+                    const float p0 = ex2_approx(x01.x);
+                    const float p1 = ex2_approx(x01.y);
+                    const float p2 = ex2_approx(x23.x);
+                    const float p3 = ex2_approx(x23.y);
+                    const int k = (c - 64 * hh) / 2;
+                    // l sums the rounded P that the MMA consumes, so O~ / l is an
+                    // exactly normalised mix of V rows even when one term dominates
+                    if constexpr (BF16) {
+                        pk[k] = pack_bf16x2(p0, p1);
+                        pk[k + 1] = pack_bf16x2(p2, p3);
+                    } else {
+                        pk[k] = pack_f16x2(p0, p1);
+                        pk[k + 1] = pack_f16x2(p2, p3);
+                    }
+                    lr01 = fadd2(lr01, unpack2<BF16>(pk[k]));
+                    lr23 = fadd2(lr23, unpack2<BF16>(pk[k + 1]));
+                    le01 = fadd2(le01, make_float2(p0, p1));
+                    le23 = fadd2(le23, make_float2(p2, p3));
                 }
-                lr01 = fadd2(lr01, unpack2<BF16>(pk[c / 2]));
-                lr23 = fadd2(lr23, unpack2<BF16>(pk[c / 2 + 1]));
-                le01 = fadd2(le01, make_float2(p0, p1));
-                le23 = fadd2(le23, make_float2(p2, p3));
+                // P of keys 64 hh .. + 63 -> columns 32 hh .. + 31 of this row's S,
+                // all of which have been read
+                tmem_st_x32(lane_base + col_s + 32 * hh, pk);
             }
             l_sum += (lr01.x + lr01.y) + (lr23.x + lr23.y);
             l_exact += (le01.x + le01.y) + (le23.x + le23.y);
-            __syncwarp();  // reconverge after the per-row branches above
-            const uint32_t p_addr = lane_base + kColS + sb * kBN;  // P overlays the S row just read
-            tmem_st_x32(p_addr, pk);
-            tmem_st_x32(p_addr + 32, pk + 32);
-
-            if (j >= 1) {
-                // O holds P_0..P_{j-1} contributions once PV_{j-1} completes
-                const bool got_o = mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status, 8);
-                if (!__all_sync(0xffffffffu, got_o)) { ok = false; break; }
-                // warp-uniform branch; lanes that keep their max use alpha = 1
-                if (__any_sync(0xffffffffu, rescale)) {
-                    tc_fence_after();
+            // O_x already holds P_x(0..j-1) V (S_x(j) was issued after the last
+            // P.V of this tile), and P_x(j) V is issued only after p_full;
+            // warp-uniform branch, lanes that keep their max use alpha = 1
+            if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld_x32(lane_base + kColO + c0, o);
-                        tmem_ld_wait_x32(o);
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld_x32(lane_base + col_o + c0, o);
+                    tmem_ld_wait_x32(o);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                        tmem_st_x32(lane_base + kColO + c0, o);
-                    }
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tmem_st_x32(lane_base + col_o + c0, o);
                 }
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_full[sb]);
+            mbar_arrive(&p_full[x]);
         }
 
-        if (ok && nkv > 0) ok = mbar_wait(o_done, (nkv - 1) & 1, abort_flag, p.status, 9);
-        __syncwarp();
-        // uniform decision across the 128 softmax threads (the epilogue has a
-        // named barrier that all of them must reach)
-        ok = named_bar_and(1, kBM, ok);
-        if (ok) {
-            tc_fence_after();
-            // Epilogue: O = O~ / l, staged through the (now idle) Q buffer in
-            // the 128-byte-swizzled layout of the output TMA box.
-            const float inv_l = 1.0f / l_sum;
-            uint8_t *stage = smem + L::OFF_Q;
+        if (nx > 0) {  // uniform across the warpgroup
+            if (ok) ok = mbar_wait(&o_final[x], 0, abort_flag, p.status, 9);
+            __syncwarp();
+            // uniform decision across the tile's 128 threads (the epilogue has a
+            // named barrier that all of them must reach)
+            ok = named_bar_and(1 + x, kBM, ok);
+            if (ok) {
+                tc_fence_after();
+                // Epilogue: O = O~ / l, staged through the (now idle) Q buffer of
+                // this tile in the 128-byte-swizzled layout of the output TMA box.
+                const float inv_l = 1.0f / l_sum;
+                uint8_t *stage = smem + L::OFF_Q + x * L::TILE;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t o[32];
-                tmem_ld_x32(lane_base + kColO + c0, o);
-                tmem_ld_wait_x32(o);
-                uint32_t w[16];
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld_x32(lane_base + col_o + c0, o);
+                    tmem_ld_wait_x32(o);
+                    uint32_t w[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float a = __uint_as_float(o[2 * c]) * inv_l;
-                    const float bb = __uint_as_float(o[2 * c + 1]) * inv_l;
-                    w[c] = BF16 ? pack_bf16x2(a, bb) : pack_f16x2(a, bb);
-                }
-                const int box = c0 >> 6;
-                uint8_t *rowp = stage + box * (kBM * 128) + row * 128;
+                    for (int c = 0; c < 16; ++c) {
+                        const float a = __uint_as_float(o[2 * c]) * inv_l;
+                        const float bb = __uint_as_float(o[2 * c + 1]) * inv_l;
+                        w[c] = BF16 ? pack_bf16x2(a, bb) : pack_f16x2(a, bb);
+                    }
+                    uint8_t *rowp = stage + (c0 >> 6) * L::BOX + row * 128;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = ((c0 & 63) >> 3) + q;
-                    uint4 val = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-                    *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (row & 7)) << 4)) = val;
+                    for (int q = 0; q < 4; ++q) {
+                        const int chunk = ((c0 & 63) >> 3) + q;
+                        *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (row & 7)) << 4)) =
+                            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    }
                 }
+                fence_proxy_async_smem();
+                named_bar_sync(1 + x, kBM);
+                if (row == 0) {
+                    for (int bx = 0; bx < L::NBOX; ++bx) tma_store_3d(&tm_o, stage + bx * L::BOX, bx * 64, q0, q_plane);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
+                if (q0 + row < p.N)
+                    p.lse[(size_t)q_plane * p.N + q0 + row] = (m_ref + log2f(l_exact)) * 0.69314718055994530942f;
             }
-            fence_proxy_async_smem();
-            named_bar_sync(1, kBM);
-            if (row == 0) {
-                for (int bx = 0; bx < L::NBOX; ++bx)
-                    tma_store_3d(&tm_o, stage + bx * (kBM * 128), bx * 64, q0, q_plane);
-                bulk_commit();
-                bulk_wait_read_all();
-            }
-            if (q0 + row < p.N)
-                p.lse[(size_t)q_plane * p.N + q0 + row] = (m_ref + log2f(l_exact)) * 0.69314718055994530942f;
         }
         __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -441,10 +445,10 @@ cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t st) {
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.N = a.N;
-    p.nqt = (a.N + kBM - 1) / kBM;
+    p.nblk = (a.N + 2 * kBM - 1) / (2 * kBM);
     p.causal = a.causal;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const long long grid = (long long)p.nqt * a.B * a.Hq;
+    const long long grid = (long long)p.nblk * a.B * a.Hq;
     fwd_kernel<D, BF16><<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
