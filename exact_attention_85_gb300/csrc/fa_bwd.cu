@@ -350,10 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (kv > q_first + r) p0 = 0.0f;
                         if (kv > q_first + r + 1) p1 = 0.0f;
                     }
-                    if (kv_oob) {
-                        p0 = 0.0f;
-                        p1 = 0.0f;
-                    }
                     const float2 t = fsub2(make_float2(__uint_as_float(dp[r]), __uint_as_float(dp[r + 1])),
                                            *reinterpret_cast<const float2 *>(dsm + r));
                     const float2 ds = fmul2(make_float2(p0, p1), t);
@@ -363,6 +359,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         pp[r / 2] = pack_f16x2(p0, p1);
                         dd[r / 2] = pack_f16x2(ds.x, ds.y);
+                    }
+                }
+                if (kv_oob) {  // P = 0, hence dS = 0, for the whole row
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        pp[r] = 0u;
+                        dd[r] = 0u;
                     }
                 }
                 __syncwarp();
