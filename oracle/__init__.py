@@ -66,10 +66,10 @@ def _load():
             lib = ctypes.CDLL(_LIB_PATH)
             P = ctypes.c_void_p
             L = ctypes.c_long
-            lib.oracle_fwd.argtypes = [P, P, P, P, P, L, L, L, L, L, ctypes.c_int, ctypes.c_double]
-            lib.oracle_fwd_rows.argtypes = [P, P, P, P, L, P, P, L, L, L, L, L, ctypes.c_int, ctypes.c_double]
-            lib.oracle_bwd_group.argtypes = [P, P, P, P, L, L, P, P, P, L, L, L, L, L, ctypes.c_int, ctypes.c_double]
-            lib.oracle_bwd.argtypes = [P, P, P, P, P, P, P, L, L, L, L, L, ctypes.c_int, ctypes.c_double]
+            lib.oracle_fwd.argtypes = [P, P, P, P, P, L, L, L, L, L, ctypes.c_int, L, ctypes.c_double]
+            lib.oracle_fwd_rows.argtypes = [P, P, P, P, L, P, P, L, L, L, L, L, ctypes.c_int, L, ctypes.c_double]
+            lib.oracle_bwd_group.argtypes = [P, P, P, P, L, L, P, P, P, L, L, L, L, L, ctypes.c_int, L, ctypes.c_double]
+            lib.oracle_bwd.argtypes = [P, P, P, P, P, P, P, L, L, L, L, L, ctypes.c_int, L, ctypes.c_double]
             lib.oracle_hadamard.argtypes = [P, P, P, L, L]
             lib.oracle_e4m3_round.argtypes = [P, P, L]
             for name in ("oracle_fwd", "oracle_fwd_rows", "oracle_bwd_group",
@@ -103,18 +103,19 @@ def _shapes(q, k):
     return B, Hq, Hkv, N, d
 
 
-def attention_fwd(q, k, v, causal: bool, scale: float):
-    """Return (O, L) in fp64; q [B,Hq,N,d], k/v [B,Hkv,N,d]."""
+def attention_fwd(q, k, v, causal: bool, scale: float, window: int = 0):
+    """Return (O, L) in fp64; q [B,Hq,N,d], k/v [B,Hkv,N,d].  ``window`` > 0
+    additionally hides key c from query r unless r - c < window."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, N, d = _shapes(q, k)
     o = np.empty_like(q)
     lse = np.empty((B, Hq, N), dtype=np.float64)
     _check(_load().oracle_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                              B, Hq, Hkv, N, d, int(causal), float(scale)), "oracle_fwd")
+                              B, Hq, Hkv, N, d, int(causal), int(window), float(scale)), "oracle_fwd")
     return o, lse
 
 
-def attention_fwd_rows(q, k, v, rows, causal: bool, scale: float):
+def attention_fwd_rows(q, k, v, rows, causal: bool, scale: float, window: int = 0):
     """O and L for the listed (b, h, r) rows only; returns ([n,d], [n])."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, Hkv, N, d = _shapes(q, k)
@@ -124,11 +125,11 @@ def attention_fwd_rows(q, k, v, rows, causal: bool, scale: float):
     lse = np.empty((n,), dtype=np.float64)
     _check(_load().oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(rows), n,
                                    _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
-                                   int(causal), float(scale)), "oracle_fwd_rows")
+                                   int(causal), int(window), float(scale)), "oracle_fwd_rows")
     return o, lse
 
 
-def attention_bwd(q, k, v, dO, causal: bool, scale: float):
+def attention_bwd(q, k, v, dO, causal: bool, scale: float, window: int = 0):
     """Return (dQ, dK, dV) in fp64 for loss = sum(dO o O)."""
     q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
     B, Hq, Hkv, N, d = _shapes(q, k)
@@ -137,11 +138,11 @@ def attention_bwd(q, k, v, dO, causal: bool, scale: float):
     dv = np.empty_like(v)
     _check(_load().oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(dq),
                               _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d,
-                              int(causal), float(scale)), "oracle_bwd")
+                              int(causal), int(window), float(scale)), "oracle_bwd")
     return dq, dk, dv
 
 
-def attention_bwd_group(q, k, v, dO, b: int, g: int, causal: bool, scale: float):
+def attention_bwd_group(q, k, v, dO, b: int, g: int, causal: bool, scale: float, window: int = 0):
     """Gradients of one (batch b, key/value head g) group.
 
     Returns dq [G,N,d] for query heads g*G..g*G+G-1 and dk, dv [N,d].
@@ -154,7 +155,7 @@ def attention_bwd_group(q, k, v, dO, b: int, g: int, causal: bool, scale: float)
     dv = np.empty((N, d), dtype=np.float64)
     _check(_load().oracle_bwd_group(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), int(b),
                                     int(g), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq,
-                                    Hkv, N, d, int(causal), float(scale)),
+                                    Hkv, N, d, int(causal), int(window), float(scale)),
            "oracle_bwd_group")
     return dq, dk, dv
 

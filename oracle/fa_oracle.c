@@ -8,8 +8,12 @@
  *
  * What it computes is the plain definition of attention, written out without
  * any tiling:
- *   S = scale * Q K^T, masked (causal: key c visible to query r iff c <= r),
+ *   S = scale * Q K^T, masked (causal: key c visible to query r iff c <= r;
+ *   sliding window of W keys: visible iff r - c < W, in addition),
  *   P = softmax_rows(S), O = P V, L = rowwise log-sum-exp of S (natural log).
+ * The window is the attention-mask change that sliding-window attention
+ * makes (FlashAttention-3 summary, discussion of GQA and sliding-window
+ * attention): it only restricts which keys a query sees; window 0 = none.
  * "FlashAttention-2 ... (blog.csdn.net, 3.1.1 forward formula analysis)" shows
  * that the tiled online-softmax recurrence with a single final diag(l)^-1
  * rescale reaches exactly this O and L = m + log(l); "6.2 FlashAttention V2 chi
@@ -47,40 +51,51 @@ static int args_ok(long B, long Hq, long Hkv, long N, long d) {
     return 1;
 }
 
-/* Number of keys visible to query row r. */
-static long visible_keys(long r, long N, int causal) {
-    return causal ? (r + 1 < N ? r + 1 : N) : N;
+/* Keys visible to query row r: c0 <= c < c1. */
+static void visible_keys(long r, long N, int causal, long window, long *c0,
+                         long *c1) {
+    *c1 = causal ? (r + 1 < N ? r + 1 : N) : N;
+    *c0 = (window > 0 && r - window + 1 > 0) ? r - window + 1 : 0;
 }
 
-/* One query row: s[c] = scale * q.k_c for visible c; returns max into *m. */
-static void score_row(const double *qr, const double *kh, long nvis, long d,
-                      double scale, double *s) {
-    for (long c = 0; c < nvis; ++c) {
+/* Query rows that see key c: r0 <= r < r1. */
+static void visible_rows(long c, long N, int causal, long window, long *r0,
+                         long *r1) {
+    *r0 = causal ? c : 0;
+    *r1 = (window > 0 && c + window < N) ? c + window : N;
+}
+
+/* One query row: s[c - c0] = scale * q.k_c for c0 <= c < c1. */
+static void score_row(const double *qr, const double *kh, long c0, long c1,
+                      long d, double scale, double *s) {
+    for (long c = c0; c < c1; ++c) {
         const double *kc = kh + c * d;
         double acc = 0.0;
         for (long t = 0; t < d; ++t) acc += qr[t] * kc[t];
-        s[c] = scale * acc;
+        s[c - c0] = scale * acc;
     }
 }
 
 /* Forward for one (b, hq, r): writes o_row[d] and *lse. s is scratch of N. */
 static void fwd_one_row(const double *q, const double *k, const double *v,
                         long b, long hq, long r, long Hq, long Hkv, long N,
-                        long d, int causal, double scale, double *s,
-                        double *o_row, double *lse) {
+                        long d, int causal, long window, double scale,
+                        double *s, double *o_row, double *lse) {
     long G = Hq / Hkv, hk = hq / G;
     const double *qr = q + IDX4(b, hq, r, Hq, N) * d;
     const double *kh = k + IDX4(b, hk, 0, Hkv, N) * d;
     const double *vh = v + IDX4(b, hk, 0, Hkv, N) * d;
-    long nvis = visible_keys(r, N, causal);
-    score_row(qr, kh, nvis, d, scale, s);
+    long c0, c1;
+    visible_keys(r, N, causal, window, &c0, &c1);
+    long nvis = c1 - c0;
+    score_row(qr, kh, c0, c1, d, scale, s);
     double m = -INFINITY;
     for (long c = 0; c < nvis; ++c) if (s[c] > m) m = s[c];
     double l = 0.0;
     for (long c = 0; c < nvis; ++c) { s[c] = exp(s[c] - m); l += s[c]; }
     for (long t = 0; t < d; ++t) o_row[t] = 0.0;
     for (long c = 0; c < nvis; ++c) {
-        const double *vc = vh + c * d;
+        const double *vc = vh + (c0 + c) * d;
         double p = s[c] / l;
         for (long t = 0; t < d; ++t) o_row[t] += p * vc[t];
     }
@@ -90,7 +105,7 @@ static void fwd_one_row(const double *q, const double *k, const double *v,
 /* O[B][Hq][N][d], lse[B][Hq][N] for the whole problem. */
 int oracle_fwd(const double *q, const double *k, const double *v, double *o,
                double *lse, long B, long Hq, long Hkv, long N, long d,
-               int causal, double scale) {
+               int causal, long window, double scale) {
     if (!args_ok(B, Hq, Hkv, N, d)) return 1;
     long total = B * Hq * N;
 #pragma omp parallel
@@ -99,8 +114,8 @@ int oracle_fwd(const double *q, const double *k, const double *v, double *o,
 #pragma omp for schedule(dynamic, 16)
         for (long idx = 0; idx < total; ++idx) {
             long r = idx % N, bh = idx / N, hq = bh % Hq, b = bh / Hq;
-            fwd_one_row(q, k, v, b, hq, r, Hq, Hkv, N, d, causal, scale, s,
-                        o + idx * d, lse + idx);
+            fwd_one_row(q, k, v, b, hq, r, Hq, Hkv, N, d, causal, window,
+                        scale, s, o + idx * d, lse + idx);
         }
         free(s);
     }
@@ -111,7 +126,7 @@ int oracle_fwd(const double *q, const double *k, const double *v, double *o,
 int oracle_fwd_rows(const double *q, const double *k, const double *v,
                     const long *rows, long nrows, double *o_rows,
                     double *lse_rows, long B, long Hq, long Hkv, long N, long d,
-                    int causal, double scale) {
+                    int causal, long window, double scale) {
     if (!args_ok(B, Hq, Hkv, N, d)) return 1;
     for (long i = 0; i < nrows; ++i) {
         long b = rows[3 * i], h = rows[3 * i + 1], r = rows[3 * i + 2];
@@ -123,7 +138,7 @@ int oracle_fwd_rows(const double *q, const double *k, const double *v,
 #pragma omp for schedule(dynamic, 1)
         for (long i = 0; i < nrows; ++i)
             fwd_one_row(q, k, v, rows[3 * i], rows[3 * i + 1], rows[3 * i + 2],
-                        Hq, Hkv, N, d, causal, scale, s, o_rows + i * d,
+                        Hq, Hkv, N, d, causal, window, scale, s, o_rows + i * d,
                         lse_rows + i);
         free(s);
     }
@@ -143,7 +158,7 @@ int oracle_fwd_rows(const double *q, const double *k, const double *v,
 int oracle_bwd_group(const double *q, const double *k, const double *v,
                      const double *dO, long b, long g, double *dq_g,
                      double *dk_g, double *dv_g, long B, long Hq, long Hkv,
-                     long N, long d, int causal, double scale) {
+                     long N, long d, int causal, long window, double scale) {
     if (!args_ok(B, Hq, Hkv, N, d)) return 1;
     if (b < 0 || b >= B || g < 0 || g >= Hkv) return 2;
     long G = Hq / Hkv;
@@ -161,8 +176,8 @@ int oracle_bwd_group(const double *q, const double *k, const double *v,
 #pragma omp for schedule(dynamic, 16)
         for (long idx = 0; idx < G * N; ++idx) {
             long j = idx / N, r = idx % N, hq = g * G + j;
-            fwd_one_row(q, k, v, b, hq, r, Hq, Hkv, N, d, causal, scale, s,
-                        Og + idx * d, Lg + idx);
+            fwd_one_row(q, k, v, b, hq, r, Hq, Hkv, N, d, causal, window,
+                        scale, s, Og + idx * d, Lg + idx);
             const double *dor = dO + IDX4(b, hq, r, Hq, N) * d;
             double acc = 0.0;
             for (long t = 0; t < d; ++t) acc += dor[t] * Og[idx * d + t];
@@ -181,11 +196,12 @@ int oracle_bwd_group(const double *q, const double *k, const double *v,
             const double *qr = q + IDX4(b, hq, r, Hq, N) * d;
             const double *dor = dO + IDX4(b, hq, r, Hq, N) * d;
             double *dqr = dq_g + idx * d;
-            long nvis = visible_keys(r, N, causal);
-            score_row(qr, kh, nvis, d, scale, s);
+            long c0, c1;
+            visible_keys(r, N, causal, window, &c0, &c1);
+            score_row(qr, kh, c0, c1, d, scale, s);
             for (long t = 0; t < d; ++t) dqr[t] = 0.0;
-            for (long c = 0; c < nvis; ++c) {
-                double p = exp(s[c] - Lg[idx]);
+            for (long c = c0; c < c1; ++c) {
+                double p = exp(s[c - c0] - Lg[idx]);
                 const double *vc = vh + c * d;
                 double dp = 0.0;
                 for (long t = 0; t < d; ++t) dp += dor[t] * vc[t];
@@ -207,8 +223,9 @@ int oracle_bwd_group(const double *q, const double *k, const double *v,
         for (long t = 0; t < d; ++t) { dkc[t] = 0.0; dvc[t] = 0.0; }
         for (long j = 0; j < G; ++j) {
             long hq = g * G + j;
-            long r0 = causal ? c : 0;
-            for (long r = r0; r < N; ++r) {
+            long r0, r1;
+            visible_rows(c, N, causal, window, &r0, &r1);
+            for (long r = r0; r < r1; ++r) {
                 long idx = j * N + r;
                 const double *qr = q + IDX4(b, hq, r, Hq, N) * d;
                 const double *dor = dO + IDX4(b, hq, r, Hq, N) * d;
@@ -230,7 +247,8 @@ int oracle_bwd_group(const double *q, const double *k, const double *v,
 /* Whole-problem backward: dq [B][Hq][N][d], dk/dv [B][Hkv][N][d]. */
 int oracle_bwd(const double *q, const double *k, const double *v,
                const double *dO, double *dq, double *dk, double *dv, long B,
-               long Hq, long Hkv, long N, long d, int causal, double scale) {
+               long Hq, long Hkv, long N, long d, int causal, long window,
+               double scale) {
     if (!args_ok(B, Hq, Hkv, N, d)) return 1;
     long G = Hq / Hkv;
     for (long b = 0; b < B; ++b)
@@ -239,7 +257,7 @@ int oracle_bwd(const double *q, const double *k, const double *v,
                                       dq + IDX4(b, g * G, 0, Hq, N) * d,
                                       dk + IDX4(b, g, 0, Hkv, N) * d,
                                       dv + IDX4(b, g, 0, Hkv, N) * d, B, Hq,
-                                      Hkv, N, d, causal, scale);
+                                      Hkv, N, d, causal, window, scale);
             if (rc) return rc;
         }
     return 0;

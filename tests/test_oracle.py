@@ -377,3 +377,60 @@ def test_fp8_reference_without_quantisation_error_is_exact():
     o, lse = oracle.attention_fwd(q, k, v, False, 0.01)
     o8, lse8 = oracle.fp8_reference(q, k, v, None, False, 0.01)
     np.testing.assert_allclose(o8, o, atol=1e-12)
+
+
+# ------------------------------------------------------- sliding window
+
+
+def _window_mask(N, window):
+    r = np.arange(N)[:, None]
+    c = np.arange(N)[None, :]
+    return (c <= r) & (r - c < window)
+
+
+@pytest.mark.parametrize("window", [1, 2, 5, 16, 40])
+def test_window_matches_torch_masked_sdpa(window):
+    """Sliding window = causal mask plus r - c < W; torch's SDPA with that
+    boolean mask (fp64, autograd) is the independent reference."""
+    B, Hq, Hkv, N, d = 2, 4, 2, 23, 8
+    q, k, v, dO = (_rand((B, h, N, d), s) for h, s in ((Hq, 11), (Hkv, 12), (Hkv, 13), (Hq, 14)))
+    scale = 0.9 / math.sqrt(d)
+    o, lse = oracle.attention_fwd(q, k, v, True, scale, window=window)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dO, True, scale, window=window)
+    G = Hq // Hkv
+    qt, kt, vt = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    mask = torch.tensor(_window_mask(N, window))
+    ot = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt.repeat_interleave(G, 1), vt.repeat_interleave(G, 1), attn_mask=mask, scale=scale)
+    ot.backward(torch.tensor(dO))
+    np.testing.assert_allclose(o, ot.detach().numpy(), atol=1e-12)
+    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-11)
+    from scipy.special import logsumexp
+    for b in range(B):
+        for h in range(Hq):
+            s = np.where(_window_mask(N, window), scale * q[b, h] @ k[b, h // G].T, -np.inf)
+            np.testing.assert_allclose(lse[b, h], logsumexp(s, axis=1), atol=1e-12)
+
+
+def test_window_one_closed_form():
+    """A window of one key: every query sees only itself, so O = V row for
+    row, L = its own score, dQ = dK = 0 and dV = dO (summed over a group)."""
+    B, Hq, Hkv, N, d = 1, 2, 1, 9, 4
+    q, k, v, dO = (_rand((B, h, N, d), s) for h, s in ((Hq, 21), (Hkv, 22), (Hkv, 23), (Hq, 24)))
+    o, lse = oracle.attention_fwd(q, k, v, True, 0.5, window=1)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dO, True, 0.5, window=1)
+    assert np.array_equal(o, np.repeat(v, 2, axis=1))
+    np.testing.assert_allclose(lse, 0.5 * np.einsum("bhnd,bnd->bhn", q, k[:, 0]), atol=1e-14)
+    assert np.abs(dq).max() == 0 and np.abs(dk).max() == 0
+    np.testing.assert_allclose(dv[:, 0], dO.sum(axis=1), atol=1e-14)
+
+
+def test_window_at_least_n_is_plain_causal():
+    B, Hq, Hkv, N, d = 1, 2, 2, 12, 4
+    q, k, v = (_rand((B, h, N, d), s) for h, s in ((Hq, 31), (Hkv, 32), (Hkv, 33)))
+    for w in (N, N + 7):
+        a = oracle.attention_fwd(q, k, v, True, 0.3, window=w)
+        b = oracle.attention_fwd(q, k, v, True, 0.3)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])

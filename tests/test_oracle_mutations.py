@@ -32,6 +32,9 @@ MUTANTS = {
     "hadamard_transposed_index": ("sylvester(i, j)", "sylvester(i, (j + 1) % d)"),
     "e4m3_ties_away": ("nearbyint(a / quantum)", "floor(a / quantum + 0.5)"),
     "e4m3_no_saturation": ("if (r > 448.0) r = 448.0;", ""),
+    "window_keys_off_by_one": ("r - window + 1 > 0) ? r - window + 1 : 0", "r - window > 0) ? r - window : 0"),
+    "window_rows_off_by_one": ("c + window < N) ? c + window : N", "c + window + 1 < N) ? c + window + 1 : N"),
+    "window_ignored_by_dk_dv": ("*r1 = (window > 0 && c + window < N) ? c + window : N;", "*r1 = N;"),
 }
 
 
@@ -80,6 +83,31 @@ def _battery():
         for nm, a, b in (("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
             if not np.allclose(a, b, atol=1e-10):
                 failed.append(f"bwd_{nm}_causal{causal}")
+
+    # sliding window: closed forms for windows of one and two keys
+    B, Hq, Hkv, N, d = 1, 4, 2, 7, 4
+    q, k, v, dO = (rng.standard_normal(sh) for sh in
+                   ((B, Hq, N, d), (B, Hkv, N, d), (B, Hkv, N, d), (B, Hq, N, d)))
+    scale = 0.7
+    kx, vx = np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1)
+    o1, l1 = oracle.attention_fwd(q, k, v, True, scale, window=1)
+    if not (np.allclose(o1, vx, atol=1e-14) and
+            np.allclose(l1, scale * np.einsum("bhnd,bhnd->bhn", q, kx), atol=1e-12)):
+        failed.append("window1_fwd")
+    dq1, dk1, dv1 = oracle.attention_bwd(q, k, v, dO, True, scale, window=1)
+    if not (np.allclose(dq1, 0, atol=1e-14) and np.allclose(dk1, 0, atol=1e-14) and
+            np.allclose(dv1, dO.reshape(B, Hkv, 2, N, d).sum(2), atol=1e-12)):
+        failed.append("window1_bwd")
+    o2, _ = oracle.attention_fwd(q, k, v, True, scale, window=2)
+    s_prev = scale * np.einsum("bhnd,bhnd->bhn", q[:, :, 1:], kx[:, :, :-1])
+    s_self = scale * np.einsum("bhnd,bhnd->bhn", q[:, :, 1:], kx[:, :, 1:])
+    w_prev = (1.0 / (1.0 + np.exp(s_self - s_prev)))[..., None]
+    o2_ref = np.concatenate([vx[:, :, :1], w_prev * vx[:, :, :-1] + (1 - w_prev) * vx[:, :, 1:]], axis=2)
+    if not np.allclose(o2, o2_ref, atol=1e-12):
+        failed.append("window2_fwd")
+    if not np.array_equal(oracle.attention_fwd(q, k, v, True, scale, window=N)[0],
+                          oracle.attention_fwd(q, k, v, True, scale)[0]):
+        failed.append("window_N_is_causal")
 
     from scipy.linalg import hadamard as sp_h
     for d in (8, 128):
