@@ -22,19 +22,27 @@ def _default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
 
-def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+def attention_fwd(q, k, v, causal: bool = False, scale: float | None = None, stream=None,
+                  window: int | None = None):
     """Returns (O, LSE).  q [B,Hq,N,d], k/v [B,Hkv,N,d]: contiguous CUDA
-    bf16/fp16 tensors; LSE is fp32 [B,Hq,N] (natural log)."""
+    bf16/fp16 tensors; LSE is fp32 [B,Hq,N] (natural log).  ``window`` (with
+    causal=True) limits row r to keys r - window + 1 .. r."""
     import torch
     B, Hq, N, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    _lib.fa_fwd(q, k, v, o, lse, causal, _default_scale(d) if scale is None else scale, stream)
+    sc = _default_scale(d) if scale is None else scale
+    if window is None:
+        _lib.fa_fwd(q, k, v, o, lse, causal, sc, stream)
+    else:
+        if not causal:
+            raise ValueError("a sliding window is defined on top of the causal mask")
+        _lib.fa_fwd_local(q, k, v, o, lse, window, sc, stream)
     return o, lse
 
 
 def attention_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: float | None = None,
-                  workspace=None, stream=None, deterministic: bool = False):
+                  workspace=None, stream=None, deterministic: bool = False, window: int | None = None):
     """Returns (dQ, dK, dV) from the forward's O and LSE and the incoming dO.
 
     ``deterministic=True`` forms dQ in a second pass over Q tiles instead of
@@ -47,8 +55,14 @@ def attention_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: float | None
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
-    fn = _lib.fa_bwd_two_pass if deterministic else _lib.fa_bwd
-    fn(q, k, v, o, lse, dO, dq, dk, dv, causal, _default_scale(d) if scale is None else scale, workspace, stream)
+    sc = _default_scale(d) if scale is None else scale
+    if window is not None:
+        if not causal:
+            raise ValueError("a sliding window is defined on top of the causal mask")
+        _lib.fa_bwd_local(q, k, v, o, lse, dO, dq, dk, dv, window, sc, deterministic, workspace, stream)
+    else:
+        fn = _lib.fa_bwd_two_pass if deterministic else _lib.fa_bwd
+        fn(q, k, v, o, lse, dO, dq, dk, dv, causal, sc, workspace, stream)
     return dq, dk, dv
 
 

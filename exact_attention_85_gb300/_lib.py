@@ -17,7 +17,7 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA, FA
 FA_FP16, FA_BF16 = 0, 1
 
 EXPORTS = (
-    "fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_two_pass", "fa_bwd_two_pass_workspace_bytes",
+    "fa_fwd", "fa_fwd_local", "fa_bwd_local", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_two_pass", "fa_bwd_two_pass_workspace_bytes",
     "fa_bwd_noalloc", "fa_hadamard_quant_fp8",
     "fa_hadamard_quant_workspace_bytes", "fa_fwd_fp8", "fa_get_device_status",
     "fa_selftest_bounded_wait", "fa_status_string",
@@ -45,6 +45,8 @@ def load():
         lib = ctypes.CDLL(LIB_PATH)
         P, I, F, Z, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_long
         lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
+        lib.fa_fwd_local.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
+        lib.fa_bwd_local.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, Z, P]
         lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, Z, P]
         lib.fa_bwd_two_pass.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, Z, P]
         lib.fa_bwd_two_pass_workspace_bytes.argtypes = [I, I, I, I]
@@ -60,7 +62,7 @@ def load():
         lib.fa_selftest_bounded_wait.argtypes = [I, P]
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_bwd", "fa_bwd_two_pass", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
+        for name in ("fa_fwd", "fa_fwd_local", "fa_bwd_local", "fa_bwd", "fa_bwd_two_pass", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
                      "fa_get_device_status", "fa_selftest_bounded_wait"):
             getattr(lib, name).restype = I
         _lib = lib
@@ -104,6 +106,23 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None):
     B, Hq, Hkv, N, d = _dims(q, k)
     _check("fa_fwd", load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
                                    int(causal), float(scale), _dtype_code(q), _stream(stream)))
+
+
+def fa_fwd_local(q, k, v, o, lse, window: int, scale: float, stream=None):
+    """Causal sliding-window forward: row r sees keys r - window + 1 .. r."""
+    B, Hq, Hkv, N, d = _dims(q, k)
+    _check("fa_fwd_local", load().fa_fwd_local(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
+                                               int(window), float(scale), _dtype_code(q), _stream(stream)))
+
+
+def fa_bwd_local(q, k, v, o, lse, dO, dq, dk, dv, window: int, scale: float, deterministic: bool, workspace,
+                 stream=None):
+    B, Hq, Hkv, N, d = _dims(q, k)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fa_bwd_local", load().fa_bwd_local(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d,
+        int(window), float(scale), _dtype_code(q), int(bool(deterministic)), _ptr(workspace), ws_bytes,
+        _stream(stream)))
 
 
 def fa_bwd_workspace_bytes(B: int, Hq: int, N: int, d: int) -> int:

@@ -114,6 +114,46 @@ fa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Shared validation and launch of the forward entry points (window 0: none).
+fa_status_t fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
+                       int N, int d, int causal, int window, float scale, fa_dtype_t dtype, void *stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
+    if (s != FA_OK) return s;
+    fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, dtype == FA_BF16, window};
+    return from_cuda(fa::launch_fwd(a, static_cast<cudaStream_t>(stream)));
+}
+
+// Shared validation and launch of the backward entry points: two_pass picks
+// the deterministic variant, whose workspace holds D only.
+fa_status_t bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                       const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d,
+                       int causal, int window, float scale, fa_dtype_t dtype, bool two_pass, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
+    if (s != FA_OK) return s;
+    const size_t rows = (size_t)B * Hq * N;
+    const size_t need = two_pass ? round256(rows * sizeof(float))
+                                 : round256(rows * sizeof(float)) + round256(rows * (size_t)d * sizeof(float));
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FA_ERR_WORKSPACE;
+    float *D = static_cast<float *>(workspace);
+    float *dq_acc =
+        two_pass ? nullptr
+                 : reinterpret_cast<float *>(static_cast<char *>(workspace) + round256(rows * sizeof(float)));
+    fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype == FA_BF16,
+                  window, D, dq_acc};
+    return from_cuda(fa::launch_bwd(a, static_cast<cudaStream_t>(stream), two_pass));
+}
+
 }  // namespace
 
 extern "C" {
@@ -132,14 +172,13 @@ const char *fa_status_string(fa_status_t s) {
 
 fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
                    int N, int d, int causal, float scale, fa_dtype_t dtype, void *stream) {
-    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-        return FA_ERR_INVALID_ARG;
-    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
-    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
-    if (s != FA_OK) return s;
-    fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_BF16};
-    return from_cuda(fa::launch_fwd(a, static_cast<cudaStream_t>(stream)));
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, stream);
+}
+
+fa_status_t fa_fwd_local(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                         int Hkv, int N, int d, int window, float scale, fa_dtype_t dtype, void *stream) {
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, 1, window, scale, dtype, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d) {
@@ -148,49 +187,33 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d) {
     return round256(rows * sizeof(float)) + round256(rows * (size_t)d * sizeof(float));
 }
 
-fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
-                   void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
-                   fa_dtype_t dtype, void *workspace, size_t workspace_bytes, void *stream) {
-    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
-    for (const void *p : ptrs)
-        if (!aligned16(p)) return FA_ERR_INVALID_ARG;
-    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
-    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
-    if (s != FA_OK) return s;
-    const size_t need = fa_bwd_workspace_bytes(B, Hq, N, d);
-    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return FA_ERR_WORKSPACE;
-    const size_t rows = (size_t)B * Hq * N;
-    float *D = static_cast<float *>(workspace);
-    float *dq_acc = reinterpret_cast<float *>(static_cast<char *>(workspace) + round256(rows * sizeof(float)));
-    fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_BF16,
-                  D, dq_acc};
-    return from_cuda(fa::launch_bwd(a, static_cast<cudaStream_t>(stream), false));
-}
-
 size_t fa_bwd_two_pass_workspace_bytes(int B, int Hq, int N, int d) {
     if (B < 1 || Hq < 1 || N < 1 || d < 1) return 0;
     return round256((size_t)B * Hq * N * sizeof(float));
+}
+
+fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
+                   void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                   fa_dtype_t dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, false,
+                      workspace, workspace_bytes, stream);
 }
 
 fa_status_t fa_bwd_two_pass(const void *q, const void *k, const void *v, const void *o, const float *lse,
                             const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d,
                             int causal, float scale, fa_dtype_t dtype, void *workspace, size_t workspace_bytes,
                             void *stream) {
-    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-    const void *ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
-    for (const void *p : ptrs)
-        if (!aligned16(p)) return FA_ERR_INVALID_ARG;
-    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
-    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
-    if (s != FA_OK) return s;
-    const size_t need = fa_bwd_two_pass_workspace_bytes(B, Hq, N, d);
-    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return FA_ERR_WORKSPACE;
-    fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal ? 1 : 0, scale, dtype == FA_BF16,
-                  static_cast<float *>(workspace), nullptr};
-    return from_cuda(fa::launch_bwd(a, static_cast<cudaStream_t>(stream), true));
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, true,
+                      workspace, workspace_bytes, stream);
+}
+
+fa_status_t fa_bwd_local(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                         const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d,
+                         int window, float scale, fa_dtype_t dtype, int deterministic, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, 1, window, scale, dtype,
+                      deterministic != 0, workspace, workspace_bytes, stream);
 }
 
 size_t fa_hadamard_quant_workspace_bytes(long rows, int d) {

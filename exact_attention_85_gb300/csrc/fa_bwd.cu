@@ -83,6 +83,7 @@ struct BwdParams {
     unsigned int *status;
     int Hq, Hkv, N, nkv, nq;
     int causal;
+    int window;  // > 0: query r sees keys r - window + 1 .. r only
     float scale, scale_log2;
 };
 
@@ -130,7 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = p.Hq / p.Hkv;
     const int kv0 = jt * kBKV;
     const int i_start = p.causal ? jt : 0;  // first Q tile with a row >= kv0 (equal tile sizes)
-    const int n_i = p.nq - i_start;
+    // with a sliding window of W keys the last query row that sees any key of
+    // this tile is kv0 + 127 + W - 1; later Q tiles are skipped
+    const int i_end = p.window > 0 ? min(p.nq, (kv0 + kBKV + p.window - 2) / kBQ + 1) : p.nq;
+    const int n_i = i_end - i_start;
     const int n_it = G * n_i;
 
     if (threadIdx.x == 0) {
@@ -327,6 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int q_base = (i_start + it % n_i) * kBQ;
             const bool diag = p.causal && (q_base + hf * 64 < kv0 + kBKV);
+            // some query of this half is W or more rows below some key of the tile
+            const bool wmask = p.window > 0 && (q_base + hf * 64 + 63 - kv0 >= p.window);
             uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
@@ -349,6 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (diag) {  // causal: key kv is visible to query q iff kv <= q
                         if (kv > q_first + r) p0 = 0.0f;
                         if (kv > q_first + r + 1) p1 = 0.0f;
+                    }
+                    if (wmask) {  // sliding window: visible iff q - kv < W
+                        if (q_first + r - kv >= p.window) p0 = 0.0f;
+                        if (q_first + r + 1 - kv >= p.window) p1 = 0.0f;
                     }
                     const float2 t = fsub2(make_float2(__uint_as_float(dp[r]), __uint_as_float(dp[r + 1])),
                                            *reinterpret_cast<const float2 *>(dsm + r));
@@ -583,6 +593,7 @@ struct DqParams {
     unsigned int *status;
     int Hq, Hkv, N, nq, nkv;
     int causal;
+    int window;  // > 0: query r sees keys r - window + 1 .. r only
     float scale, scale_log2;
 };
 
@@ -626,7 +637,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int h = bh - b * p.Hq;
     const int kv_plane = b * p.Hkv + h / (p.Hq / p.Hkv);
     const int q0 = qt * 128;
-    const int n_j = p.causal ? min(qt + 1, p.nkv) : p.nkv;
+    const int j_end = p.causal ? min(qt + 1, p.nkv) : p.nkv;
+    // sliding window of W keys: the first key any row of this tile sees is
+    // q0 - W + 1, so K/V tiles before its tile are skipped
+    const int j_lo = p.window > 0 ? max(0, q0 - p.window + 1) / 128 : 0;
+    const int n_j = j_end - j_lo;  // K/V tiles j_lo .. j_end - 1, counted from 0 below
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -665,14 +680,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 mbar_arrive_expect_tx(&k_full[ks], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_K + ks * L::TILE + bx * L::BOX, &tm_k, &k_full[ks], bx * 64,
-                                j * 128, kv_plane);
+                                (j_lo + j) * 128, kv_plane);
                 ++nk;
                 const int vs = j % VS;
                 if (j >= VS && !mbar_wait(&v_empty[vs], ((j / VS) + 1) & 1, abort_flag, p.status, 42)) break;
                 mbar_arrive_expect_tx(&v_full[vs], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_V + vs * L::TILE + bx * L::BOX, &tm_v, &v_full[vs], bx * 64,
-                                j * 128, kv_plane);
+                                (j_lo + j) * 128, kv_plane);
                 ++nv;
             }
             if (*abort_flag) {
@@ -764,8 +779,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         // rows past N: P = 0 (their dQ rows are not stored)
         const float nl2 = q_in ? -p.lse[(size_t)bh * p.N + q] * 1.4426950408889634f : -INFINITY;
         const float dq_d = q_in ? p.Dvec[(size_t)bh * p.N + q] : 0.0f;
-        // last key this row attends to: causal q, and never a key past N
+        // keys this row attends to: kv_lo .. kv_last (causal: up to q; never
+        // a key past N; sliding window: from q - W + 1)
         const int kv_last = p.causal ? min(q, p.N - 1) : p.N - 1;
+        const int kv_lo = p.window > 0 ? q - p.window + 1 : 0;
         const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 nl2x2 = make_float2(nl2, nl2);
         const float2 dx2 = make_float2(dq_d, dq_d);
@@ -782,8 +799,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tmem_ld_wait_x32(dp + 32);
             tc_fence_before();
             mbar_arrive(dp_free);
-            const int kv_first = j * 128 + hf * 64;
-            const bool masked = kv_first + 63 > kv_last;
+            const int kv_first = (j_lo + j) * 128 + hf * 64;
+            const bool masked = kv_first + 63 > kv_last || kv_first < kv_lo;
             const uint32_t s_cols = lane_base + kDqColS + sb * 128 + hf * 64;
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -798,8 +815,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     float p1 = ex2_approx(t.y);
                     if (masked) {
                         const int kv = kv_first + 32 * c + x;
-                        if (kv > kv_last) p0 = 0.0f;
-                        if (kv + 1 > kv_last) p1 = 0.0f;
+                        if (kv > kv_last || kv < kv_lo) p0 = 0.0f;
+                        if (kv + 1 > kv_last || kv + 1 < kv_lo) p1 = 0.0f;
                     }
                     const float2 ds = fmul2(make_float2(p0, p1),
                                             fsub2(make_float2(__uint_as_float(dp[32 * c + x]),
@@ -910,6 +927,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
     p.nkv = (a.N + kBKV - 1) / kBKV;
     p.nq = (a.N + kBQ - 1) / kBQ;
     p.causal = a.causal;
+    p.window = a.window;
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     const long long grid = (long long)p.nkv * a.B * a.Hkv;
@@ -932,6 +950,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
         pq2.nq = p.nq;
         pq2.nkv = p.nkv;
         pq2.causal = a.causal;
+        pq2.window = a.window;
         pq2.scale = a.scale;
         pq2.scale_log2 = p.scale_log2;
         const long long grid2 = (long long)p.nq * a.B * a.Hq;

@@ -70,6 +70,7 @@ struct FwdParams {
     float *lse;
     unsigned int *status;
     int Hq, Hkv, N, nblk, causal;  // nblk: 256-row blocks per head
+    int window;                    // > 0: row r sees keys r - window + 1 .. r only
     float scale_log2;              // scale * log2(e)
 };
 
@@ -113,6 +114,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nA = p.causal ? min(q0a / kBN + 1, nkv_all) : nkv_all;
     const int nB = q0a + kBM >= p.N ? 0 : (p.causal ? min((q0a + kBM) / kBN + 1, nkv_all) : nkv_all);
     const int nmax = max(nA, nB);
+    // first K/V tile each Q tile visits: with a sliding window of W keys, row
+    // r sees keys r - W + 1 .. r, so tile X starts at the tile holding key
+    // q0_X - W + 1 (the tiles before it are skipped like those above the
+    // causal diagonal)
+    const int jA0 = p.window > 0 ? max(0, q0a - p.window + 1) / kBN : 0;
+    const int jB0 = p.window > 0 ? max(0, q0a + kBM - p.window + 1) / kBN : 0;
     const int kv_plane = b * p.Hkv + hk;
     const int q_plane = b * p.Hq + h;
 
@@ -152,16 +159,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 q_plane);
             // K_j then V_j: the order in which the MMAs first need them
             int nk = 0, nv = 0;
-            for (int j = 0; j < nmax; ++j) {
-                const int ks = j % L::KS;
-                if (j >= L::KS && !mbar_wait(&k_empty[ks], ((j / L::KS) + 1) & 1, abort_flag, p.status, 1)) break;
+            for (int j = jA0; j < nmax; ++j) {
+                const int u = j - jA0;  // position in the K/V stream
+                const int ks = u % L::KS;
+                if (u >= L::KS && !mbar_wait(&k_empty[ks], ((u / L::KS) + 1) & 1, abort_flag, p.status, 1)) break;
                 mbar_arrive_expect_tx(&k_full[ks], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_K + ks * L::TILE + bx * L::BOX, &tm_k, &k_full[ks], bx * 64, j * kBN,
                                 kv_plane);
                 ++nk;
-                const int vs = j % L::VS;
-                if (j >= L::VS && !mbar_wait(&v_empty[vs], ((j / L::VS) + 1) & 1, abort_flag, p.status, 2)) break;
+                const int vs = u % L::VS;
+                if (u >= L::VS && !mbar_wait(&v_empty[vs], ((u / L::VS) + 1) & 1, abort_flag, p.status, 2)) break;
                 mbar_arrive_expect_tx(&v_full[vs], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_V + vs * L::TILE + bx * L::BOX, &tm_v, &v_full[vs], bx * 64, j * kBN,
@@ -188,20 +196,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t q_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_Q), 16, 1024);
             const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);
             const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_V), L::BOX, 1024);
-            int k_ready = -1;  // highest K tile whose arrival has been observed
+            int k_ready = -1;  // highest K/V stream position whose K arrival has been observed
 
-            auto wait_k = [&](int j) -> bool {
-                if (j <= k_ready) return true;
-                if (!mbar_wait(&k_full[j % L::KS], (j / L::KS) & 1, abort_flag, p.status, 3)) return false;
+            // u = j - jA0 is the position of K/V tile j in the stream
+            auto wait_k = [&](int u) -> bool {
+                if (u <= k_ready) return true;
+                if (!mbar_wait(&k_full[u % L::KS], (u / L::KS) & 1, abort_flag, p.status, 3)) return false;
                 tc_fence_after();
-                k_ready = j;
+                k_ready = u;
                 return true;
             };
             // S_x(j) = Q_x K_j^T (A = Q, B = K, both K-major, 32 bytes per step
             // inside a 128-byte row)
-            auto issue_s = [&](int x, int j) {
+            auto issue_s = [&](int x, int u) {
                 const uint64_t q_desc = sdesc_advance(q_desc0, x * L::TILE);
-                const uint64_t k_desc = sdesc_advance(k_desc0, (j % L::KS) * L::TILE);
+                const uint64_t k_desc = sdesc_advance(k_desc0, (u % L::KS) * L::TILE);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * L::BOX + (kk & 3) * 32;
@@ -210,17 +219,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&s_full[x]);
             };
-            // O_x += P_x(j) V_j (A = P from tensor memory, 16 keys = 8 columns
-            // per step; B = V, MN-major, 16 rows of 128 bytes per step)
-            auto issue_pv = [&](int x, int j) -> bool {
-                if (!mbar_wait(&p_full[x], j & 1, abort_flag, p.status, 4)) return false;
+            // O_x += P_x V_j (A = P from tensor memory, 16 keys = 8 columns
+            // per step; B = V, MN-major, 16 rows of 128 bytes per step); jj is
+            // the tile's own step count, u the stream position of V_j
+            auto issue_pv = [&](int x, int jj, int u) -> bool {
+                if (!mbar_wait(&p_full[x], jj & 1, abort_flag, p.status, 4)) return false;
                 tc_fence_after();
-                const uint64_t v_desc = sdesc_advance(v_desc0, (j % L::VS) * L::TILE);
+                const uint64_t v_desc = sdesc_advance(v_desc0, (u % L::VS) * L::TILE);
                 const uint32_t p_col = tmem + kColS + x * 128;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
                     mma_f16_ts(tmem + kColO + x * 128, p_col + kk * 8, sdesc_advance(v_desc, kk * 2048), idesc_pv,
-                               (j > 0 || kk > 0) ? 1u : 0u);
+                               (jj > 0 || kk > 0) ? 1u : 0u);
                 return true;
             };
 
@@ -228,27 +238,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) ok = wait_k(0);
             if (ok) {
                 issue_s(0, 0);
-                if (nB > 0) issue_s(1, 0);
+                if (nB > 0 && jB0 == jA0) issue_s(1, 0);
                 mma_commit(&k_empty[0]);
             }
-            for (int j = 0; ok && j < nmax; ++j) {
-                if (!mbar_wait(&v_full[j % L::VS], (j / L::VS) & 1, abort_flag, p.status, 6)) { ok = false; break; }
+            for (int j = jA0; ok && j < nmax; ++j) {
+                const int u = j - jA0;
+                if (!mbar_wait(&v_full[u % L::VS], (u / L::VS) & 1, abort_flag, p.status, 6)) { ok = false; break; }
                 tc_fence_after();
                 for (int x = 0; x < 2; ++x) {
                     const int nx = x ? nB : nA;
-                    if (j >= nx) continue;
-                    if (!issue_pv(x, j)) { ok = false; break; }
+                    const int jx0 = x ? jB0 : jA0;
+                    if (j < jx0 - 1 || j >= nx) continue;
+                    if (j >= jx0) {
+                        if (!issue_pv(x, j - jx0, u)) { ok = false; break; }
+                        if (j + 1 == nx) mma_commit(&o_final[x]);
+                    }
                     if (j + 1 < nx) {
                         // S_x(j+1) overwrites P_x(j), which the MMAs just issued read first
-                        if (!wait_k(j + 1)) { ok = false; break; }
-                        issue_s(x, j + 1);
-                    } else {
-                        mma_commit(&o_final[x]);
+                        if (!wait_k(u + 1)) { ok = false; break; }
+                        issue_s(x, u + 1);
                     }
                 }
                 if (!ok) break;
-                mma_commit(&v_empty[j % L::VS]);
-                if (j + 1 < nmax) mma_commit(&k_empty[(j + 1) % L::KS]);
+                mma_commit(&v_empty[u % L::VS]);
+                if (j + 1 < nmax) mma_commit(&k_empty[(u + 1) % L::KS]);
             }
             // every MMA issued above has completed once `drain` flips
             mma_commit(drain);
@@ -264,16 +277,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t col_s = kColS + x * 128, col_o = kColO + x * 128;
         const int q0 = q0a + x * kBM;
         const int nx = x ? nB : nA;
+        const int jx0 = x ? jB0 : jA0;
         const float sl2 = p.scale_log2;
         float m_ref = -INFINITY;
         float l_sum = 0.0f;    // sum of the rounded P fed to the MMA: normalises O
         float l_exact = 0.0f;  // sum of the unrounded P: gives L
         bool ok = true;
 
-        for (int j = 0; ok && j < nx; ++j) {
+        for (int j = jx0; ok && j < nx; ++j) {
+            const int jj = j - jx0;  // this tile's own step count
             // every lane waits, then the warp votes: the tcgen05.ld/st below
             // are warp-collective (.sync.aligned) and need all 32 lanes
-            const bool got_s = mbar_wait(&s_full[x], j & 1, abort_flag, p.status, 7);
+            const bool got_s = mbar_wait(&s_full[x], jj & 1, abort_flag, p.status, 7);
             if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
             tc_fence_after();
             uint32_t s[128];
@@ -288,12 +303,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait_x32(s + 96);
 
             const int kv0 = j * kBN;
-            const bool need_mask = (kv0 + kBN > p.N) || (p.causal && kv0 + kBN - 1 > q0);
+            const bool need_mask = (kv0 + kBN > p.N) || (p.causal && kv0 + kBN - 1 > q0) ||
+                                   (p.window > 0 && kv0 < q0 + kBM - p.window);
             if (need_mask) {
-                const int lim = p.causal ? min(p.N, q0 + row + 1) : p.N;  // visible: col < lim
+                // visible: lo <= key < hi
+                const int hi = p.causal ? min(p.N, q0 + row + 1) : p.N;
+                const int lo = p.window > 0 ? q0 + row - p.window + 1 : 0;
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
-                    if (kv0 + c >= lim) s[c] = __float_as_uint(-INFINITY);
+                    if (kv0 + c >= hi || kv0 + c < lo) s[c] = __float_as_uint(-INFINITY);
             }
             // four chains of three-input maxima: two new scores per instruction
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
@@ -315,7 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rescale = true;
             }
             __syncwarp();  // reconverge after the per-row branches above
-            const float2 neg_m = make_float2(-m_ref, -m_ref);
+            // a row that has seen no visible key yet (its keys start in a later
+            // tile of a sliding window) keeps m_ref = -inf: use 0 so that its
+            // masked scores give P = 0 rather than -inf - (-inf)
+            const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
+            const float2 neg_m = make_float2(-m_use, -m_use);
             const float2 sl2x2 = make_float2(sl2, sl2);
             float2 lr01 = make_float2(0.f, 0.f), lr23 = lr01, le01 = lr01, le23 = lr01;
 #pragma unroll
@@ -355,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // O_x already holds P_x(0..j-1) V (S_x(j) was issued after the last
             // P.V of this tile), and P_x(j) V is issued only after p_full;
             // warp-uniform branch, lanes that keep their max use alpha = 1
-            if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+            if (jj >= 1 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 32) {
                     uint32_t o[32];
@@ -447,6 +469,7 @@ cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t st) {
     p.N = a.N;
     p.nblk = (a.N + 2 * kBM - 1) / (2 * kBM);
     p.causal = a.causal;
+    p.window = a.window;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     const long long grid = (long long)p.nblk * a.B * a.Hq;
     fwd_kernel<D, BF16><<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, to, p);

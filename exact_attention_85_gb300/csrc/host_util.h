@@ -26,6 +26,7 @@ struct FwdArgs {
     int B, Hq, Hkv, N, d, causal;
     float scale;
     bool bf16;
+    int window;  // 0: none; > 0: causal sliding window of that many keys
 };
 
 struct BwdArgs {
@@ -35,6 +36,7 @@ struct BwdArgs {
     int B, Hq, Hkv, N, d, causal;
     float scale;
     bool bf16;
+    int window;    // 0: none; > 0: causal sliding window of that many keys
     float *D;      // [B][Hq][N]
     float *dq_acc; // [B][Hq][N][d]; unused (may be null) by the two-pass backward
 };

@@ -67,6 +67,23 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
                    int causal, float scale, fa_dtype_t dtype, void *stream);
 
 /*
+ * Causal sliding-window ("local") forward: fa_fwd with causal = 1 and the
+ * additional mask that query row r sees only the `window` most recent keys,
+ * r - window + 1 .. r (its own key included).
+ * [FA3] discussion of GQA and sliding-window attention (sliding-window
+ * attention changes the attention mask, i.e. which queries see which keys;
+ * the algorithm is otherwise unchanged); [V2] section 5.3 (tiles that lie
+ * wholly outside the mask are skipped, boundary tiles are masked
+ * element-wise) applied to the window's lower edge as well.
+ *   Arguments, layouts and results as fa_fwd; window >= 1 (window >= N is
+ *   plain causal attention), otherwise FA_ERR_INVALID_ARG.
+ */
+fa_status_t fa_fwd_local(const void *q, const void *k, const void *v, void *o,
+                         float *lse, int B, int Hq, int Hkv, int N, int d,
+                         int window, float scale, fa_dtype_t dtype,
+                         void *stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: D (B*Hq*N fp32, rounded up to 256
  * bytes) followed by the fp32 dQ accumulator (B*Hq*N*d fp32).
  */
@@ -122,6 +139,24 @@ fa_status_t fa_bwd_two_pass(const void *q, const void *k, const void *v,
                             int Hkv, int N, int d, int causal, float scale,
                             fa_dtype_t dtype, void *workspace,
                             size_t workspace_bytes, void *stream);
+
+/*
+ * Backward of fa_fwd_local (same sliding-window mask), from O, LSE and dO.
+ * [CSDN] 3.1.2 and [V2] section 7 as for fa_bwd, with the mask of
+ * fa_fwd_local; K/V column blocks visit only the Q row blocks that see them
+ * and Q row blocks only the K/V blocks they see.
+ *   Arguments and layouts as fa_bwd; window >= 1.
+ *   deterministic = 0: dQ by fp32 atomic addition (as fa_bwd), workspace of
+ *   at least fa_bwd_workspace_bytes(B,Hq,N,d) bytes;
+ *   deterministic = 1: dQ by a second pass (as fa_bwd_two_pass), workspace
+ *   of at least fa_bwd_two_pass_workspace_bytes(B,Hq,N,d) bytes.
+ */
+fa_status_t fa_bwd_local(const void *q, const void *k, const void *v,
+                         const void *o, const float *lse, const void *dO,
+                         void *dq, void *dk, void *dv, int B, int Hq, int Hkv,
+                         int N, int d, int window, float scale,
+                         fa_dtype_t dtype, int deterministic, void *workspace,
+                         size_t workspace_bytes, void *stream);
 
 /*
  * Size of the scratch buffer built into the library for fa_bwd_noalloc:
