@@ -41,6 +41,7 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-two-pass", action="store_true", help="skip the deterministic two-pass backward leg")
+    ap.add_argument("--no-window", action="store_true", help="skip the sliding-window leg")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 leg (outlier workload)")
     return ap.parse_args()
 
@@ -262,6 +263,8 @@ def run_ours(a):
     if has_bwd and not a.no_two_pass:
         result["two_pass_bwd_leg"] = _two_pass_leg(a, w, (q, k, v, o, lse, dO, dq, dk, dv), dev, stream, peaks,
                                                    flush)
+    if has_bwd and not a.no_window and w.causal:
+        result["window_leg"] = _window_leg(a, w, (q, k, v, o, lse, dO, dq, dk, dv), dev, stream, peaks, flush)
     if not a.no_fp8 and a.workload is None:
         result["fp8_leg"] = _fp8_leg(a, dev, stream, peaks)
     if not a.no_e2e:
@@ -309,6 +312,56 @@ def _two_pass_leg(a, w, t, dev, stream, peaks, flush):
     return {"workload": w.name, "bwd_ms": round(ms, 4), "bwd_tflops": round(tf, 1),
             "bwd_frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
             "executed_tflops": round(tf * 7.0 / 5.0, 1), "launches_per_step": 3, "deterministic": True}
+
+
+def _window_leg(a, w, t, dev, stream, peaks, flush, window=1024):
+    """Causal sliding-window attention (fa_fwd_local / fa_bwd_local, atomic
+    dQ) on the step's workload with a window of `window` keys.  FLOPs count
+    the visible (query, key) pairs only: sum over rows of min(r + 1, W)."""
+    import torch
+
+    from exact_attention_85_gb300 import _lib
+
+    q, k, v, o, lse, dO, dq, dk, dv = t
+    B, Hq, N, d = q.shape
+    ws = torch.empty(_lib.fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device=dev)
+    W = min(window, N)
+    pairs = W * (W + 1) / 2 + (N - W) * W
+    f_fwd = 4.0 * B * Hq * d * pairs
+    f_bwd = 2.5 * f_fwd
+
+    def fwd():
+        _lib.fa_fwd_local(q, k, v, o, lse, W, w.scale, stream)
+
+    def bwd():
+        _lib.fa_bwd_local(q, k, v, o, lse, dO, dq, dk, dv, W, w.scale, False, ws, stream)
+
+    for _ in range(max(3, a.warmup)):
+        fwd()
+        bwd()
+        flush.zero_()
+    torch.cuda.synchronize()
+    steps = max(3, min(a.steps, 10))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if _lib.fa_get_device_status(stream) != _lib.FA_OK:
+        raise RuntimeError("a bounded device wait ran out during the sliding-window leg")
+    f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    b_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ftf = f_fwd / (f_ms * 1e-3) / 1e12
+    btf = f_bwd / (b_ms * 1e-3) / 1e12
+    return {"workload": f"{w.name} window={W}", "fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4),
+            "fwd_tflops": round(ftf, 1), "bwd_tflops": round(btf, 1),
+            "fwd_frac_of_peak": round(ftf / peaks["bf16_tflops"], 4),
+            "bwd_frac_of_peak": round(btf / peaks["bf16_tflops"], 4), "launches_per_step": 4,
+            "flops": "visible (query, key) pairs only"}
 
 
 def _fp8_leg(a, dev, stream, peaks):

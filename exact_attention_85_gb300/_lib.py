@@ -17,7 +17,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_WORKSPACE, FA_ERR_CUDA, FA
 FA_FP16, FA_BF16 = 0, 1
 
 EXPORTS = (
-    "fa_fwd", "fa_fwd_local", "fa_bwd_local", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_two_pass", "fa_bwd_two_pass_workspace_bytes",
+    "fa_fwd", "fa_fwd_local", "fa_bwd_local", "fa_fwd_varlen", "fa_bwd_varlen", "fa_bwd_varlen_workspace_bytes",
+    "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_two_pass", "fa_bwd_two_pass_workspace_bytes",
     "fa_bwd_noalloc", "fa_hadamard_quant_fp8",
     "fa_hadamard_quant_workspace_bytes", "fa_fwd_fp8", "fa_get_device_status",
     "fa_selftest_bounded_wait", "fa_status_string",
@@ -47,6 +48,10 @@ def load():
         lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_fwd_local.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_bwd_local.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, Z, P]
+        lib.fa_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P]
+        lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, Z, P]
+        lib.fa_bwd_varlen_workspace_bytes.argtypes = [I, I, I, I]
+        lib.fa_bwd_varlen_workspace_bytes.restype = Z
         lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, Z, P]
         lib.fa_bwd_two_pass.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, Z, P]
         lib.fa_bwd_two_pass_workspace_bytes.argtypes = [I, I, I, I]
@@ -62,7 +67,7 @@ def load():
         lib.fa_selftest_bounded_wait.argtypes = [I, P]
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_local", "fa_bwd_local", "fa_bwd", "fa_bwd_two_pass", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
+        for name in ("fa_fwd", "fa_fwd_local", "fa_bwd_local", "fa_fwd_varlen", "fa_bwd_varlen", "fa_bwd", "fa_bwd_two_pass", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
                      "fa_get_device_status", "fa_selftest_bounded_wait"):
             getattr(lib, name).restype = I
         _lib = lib
@@ -123,6 +128,34 @@ def fa_bwd_local(q, k, v, o, lse, dO, dq, dk, dv, window: int, scale: float, det
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d,
         int(window), float(scale), _dtype_code(q), int(bool(deterministic)), _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen: int, causal: bool, scale: float, window: int = 0,
+                  stream=None):
+    """Packed sequences: q/o [total,Hq,d], k/v [total,Hkv,d], lse [Hq,total],
+    cu_seqlens int32 [B+1] on the device."""
+    total, Hq, d = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.numel() - 1
+    _check("fa_fwd_varlen", load().fa_fwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), B, int(max_seqlen), total, Hq, Hkv, d,
+        int(causal), int(window), float(scale), _dtype_code(q), _stream(stream)))
+
+
+def fa_bwd_varlen_workspace_bytes(total: int, Hq: int, d: int, deterministic: bool) -> int:
+    return int(load().fa_bwd_varlen_workspace_bytes(total, Hq, d, int(bool(deterministic))))
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens, max_seqlen: int, causal: bool, scale: float,
+                  deterministic: bool, workspace, window: int = 0, stream=None):
+    total, Hq, d = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.numel() - 1
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("fa_bwd_varlen", load().fa_bwd_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens),
+        B, int(max_seqlen), total, Hq, Hkv, d, int(causal), int(window), float(scale), _dtype_code(q),
+        int(bool(deterministic)), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def fa_bwd_workspace_bytes(B: int, Hq: int, N: int, d: int) -> int:

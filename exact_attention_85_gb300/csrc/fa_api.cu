@@ -56,19 +56,34 @@ __global__ void selftest_wait_kernel(unsigned int *status, unsigned long long li
 
 }  // namespace
 
-bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, uint64_t dim0,
-                  uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle) {
+bool make_tmap_3d_box(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, uint64_t dim0,
+                      uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1, uint32_t box2,
+                      CUtensorMapSwizzle swizzle) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {dim0, dim1, dim2};
     cuuint64_t strides[2] = {dim0 * elem_bytes, dim0 * dim1 * elem_bytes};
-    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t box[3] = {box0, box1, box2};
     cuuint32_t estr[3] = {1, 1, 1};
     std::memset(map, 0, sizeof(*map));
     CUresult r = enc(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes, uint64_t dim0,
+                  uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle) {
+    return make_tmap_3d_box(map, base, dtype, elem_bytes, dim0, dim1, dim2, box0, box1, 1, swizzle);
+}
+
+bool make_tmap_tiles(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int d, const SeqLayout &lay,
+                     int heads, uint32_t rows) {
+    if (lay.varlen)  // [total][heads][d]: coordinates (column, head, token)
+        return make_tmap_3d_box(map, base, dtype, 2, d, heads, lay.total, 64, 1, rows, CU_TENSOR_MAP_SWIZZLE_128B);
+    // [B * heads][N][d]: coordinates (column, row, plane)
+    return make_tmap_3d_box(map, base, dtype, 2, d, lay.N, (uint64_t)lay.B * heads, 64, rows, 1,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 unsigned int *device_status_ptr() {
@@ -116,14 +131,17 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Shared validation and launch of the forward entry points (window 0: none).
 fa_status_t fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
-                       int N, int d, int causal, int window, float scale, fa_dtype_t dtype, void *stream) {
+                       int N, int d, int causal, int window, float scale, fa_dtype_t dtype, void *stream,
+                       const fa::SeqLayout *packed = nullptr) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
     fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
     if (s != FA_OK) return s;
-    fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, dtype == FA_BF16, window};
+    fa::SeqLayout lay{0, B, N, B * N, nullptr};
+    if (packed) lay = *packed;
+    fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, dtype == FA_BF16, window, lay};
     return from_cuda(fa::launch_fwd(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -132,7 +150,7 @@ fa_status_t fwd_common(const void *q, const void *k, const void *v, void *o, flo
 fa_status_t bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse,
                        const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d,
                        int causal, int window, float scale, fa_dtype_t dtype, bool two_pass, void *workspace,
-                       size_t workspace_bytes, void *stream) {
+                       size_t workspace_bytes, void *stream, const fa::SeqLayout *packed = nullptr) {
     if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv};
     for (const void *p : ptrs)
@@ -140,7 +158,9 @@ fa_status_t bwd_common(const void *q, const void *k, const void *v, const void *
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
     fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
     if (s != FA_OK) return s;
-    const size_t rows = (size_t)B * Hq * N;
+    fa::SeqLayout lay{0, B, N, B * N, nullptr};
+    if (packed) lay = *packed;
+    const size_t rows = (size_t)lay.total * Hq;
     const size_t need = two_pass ? round256(rows * sizeof(float))
                                  : round256(rows * sizeof(float)) + round256(rows * (size_t)d * sizeof(float));
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -150,7 +170,7 @@ fa_status_t bwd_common(const void *q, const void *k, const void *v, const void *
         two_pass ? nullptr
                  : reinterpret_cast<float *>(static_cast<char *>(workspace) + round256(rows * sizeof(float)));
     fa::BwdArgs a{q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype == FA_BF16,
-                  window, D, dq_acc};
+                  window, lay, D, dq_acc};
     return from_cuda(fa::launch_bwd(a, static_cast<cudaStream_t>(stream), two_pass));
 }
 
@@ -216,6 +236,46 @@ fa_status_t fa_bwd_local(const void *q, const void *k, const void *v, const void
                       deterministic != 0, workspace, workspace_bytes, stream);
 }
 
+namespace {
+// Checks shared by the packed (variable-length) entry points.
+fa_status_t check_varlen(const int *cu_seqlens, int B, int max_seqlen, int total, int Hq, int Hkv, int d,
+                         int causal, int window) {
+    if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_INVALID_ARG;
+    if (B < 1 || max_seqlen < 1 || total < 1 || Hq < 1 || Hkv < 1) return FA_ERR_INVALID_ARG;
+    if (window < 0 || (window > 0 && !causal)) return FA_ERR_INVALID_ARG;
+    if ((long long)total * (Hq > Hkv ? Hq : Hkv) * d > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
+}  // namespace
+
+fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu_seqlens,
+                          int B, int max_seqlen, int total, int Hq, int Hkv, int d, int causal, int window,
+                          float scale, fa_dtype_t dtype, void *stream) {
+    fa_status_t s = check_varlen(cu_seqlens, B, max_seqlen, total, Hq, Hkv, d, causal, window);
+    if (s != FA_OK) return s;
+    const fa::SeqLayout lay{1, B, max_seqlen, total, cu_seqlens};
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, max_seqlen, d, causal ? 1 : 0, window, scale, dtype, stream,
+                      &lay);
+}
+
+size_t fa_bwd_varlen_workspace_bytes(int total, int Hq, int d, int deterministic) {
+    if (total < 1 || Hq < 1 || d < 1) return 0;
+    const size_t rows = (size_t)total * Hq;
+    return round256(rows * sizeof(float)) + (deterministic ? 0 : round256(rows * (size_t)d * sizeof(float)));
+}
+
+fa_status_t fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                          const void *dO, void *dq, void *dk, void *dv, const int *cu_seqlens, int B,
+                          int max_seqlen, int total, int Hq, int Hkv, int d, int causal, int window, float scale,
+                          fa_dtype_t dtype, int deterministic, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    fa_status_t s = check_varlen(cu_seqlens, B, max_seqlen, total, Hq, Hkv, d, causal, window);
+    if (s != FA_OK) return s;
+    const fa::SeqLayout lay{1, B, max_seqlen, total, cu_seqlens};
+    return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, max_seqlen, d, causal ? 1 : 0, window, scale,
+                      dtype, deterministic != 0, workspace, workspace_bytes, stream, &lay);
+}
+
 size_t fa_hadamard_quant_workspace_bytes(long rows, int d) {
     (void)rows;
     (void)d;
@@ -258,7 +318,8 @@ fa_status_t fa_get_device_status(void *stream) {
     if (cudaMemcpyAsync(&host, p, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess) return FA_ERR_CUDA;
     if (cudaMemsetAsync(p, 0, sizeof(unsigned int), st) != cudaSuccess) return FA_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
-    return (host & fa::kStatusTimeout) ? FA_ERR_TIMEOUT : FA_OK;
+    if (host & fa::kStatusTimeout) return FA_ERR_TIMEOUT;
+    return (host & fa::kStatusBadArgs) ? FA_ERR_INVALID_ARG : FA_OK;
 }
 
 fa_status_t fa_selftest_bounded_wait(int timeout_us, void *stream) {

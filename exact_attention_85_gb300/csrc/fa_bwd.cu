@@ -80,7 +80,10 @@ struct BwdParams {
     const float *lse;
     const float *Dvec;
     float *dq_acc;
+    void *dk, *dv;           // packed layout: stored row by row
     unsigned int *status;
+    const int *cu_seqlens;   // packed layout: sequence b is rows cu[b] .. cu[b+1]-1
+    int varlen, total;
     int Hq, Hkv, N, nkv, nq;
     int causal;
     int window;  // > 0: query r sees keys r - window + 1 .. r only
@@ -130,10 +133,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = bg - b * p.Hkv;
     const int G = p.Hq / p.Hkv;
     const int kv0 = jt * kBKV;
+    // rows of this sequence (packed layout: rows row0 .. row0 + N - 1 of the
+    // token-major tensors)
+    int N = p.N, row0 = 0;
+    if (p.varlen) {
+        row0 = p.cu_seqlens[b];
+        N = p.cu_seqlens[b + 1] - row0;
+        if (N < 0 || N > p.N || row0 < 0 || row0 + N > p.total) {
+            if (threadIdx.x == 0 && jt == 0) record_bad_args(p.status);
+            return;  // uniform across the CTA, nothing started yet
+        }
+    }
+    if (kv0 >= N) return;  // key tile past the end of a shorter sequence
+    const int nq = (N + kBQ - 1) / kBQ;
     const int i_start = p.causal ? jt : 0;  // first Q tile with a row >= kv0 (equal tile sizes)
     // with a sliding window of W keys the last query row that sees any key of
     // this tile is kv0 + 127 + W - 1; later Q tiles are skipped
-    const int i_end = p.window > 0 ? min(p.nq, (kv0 + kBKV + p.window - 2) / kBQ + 1) : p.nq;
+    const int i_end = p.window > 0 ? min(nq, (kv0 + kBKV + p.window - 2) / kBQ + 1) : nq;
     const int n_i = i_end - i_start;
     const int n_it = G * n_i;
 
@@ -173,8 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_do);
             mbar_arrive_expect_tx(kv_full, 2 * L::TILE_KV);
             for (int bx = 0; bx < L::NBOX; ++bx) {
-                tma_load_3d(smem + L::OFF_K + bx * L::BOX_KV, &tm_k, kv_full, bx * 64, kv0, bg);
-                tma_load_3d(smem + L::OFF_V + bx * L::BOX_KV, &tm_v, kv_full, bx * 64, kv0, bg);
+                const int c1 = p.varlen ? g : kv0, c2 = p.varlen ? row0 + kv0 : bg;
+                tma_load_3d(smem + L::OFF_K + bx * L::BOX_KV, &tm_k, kv_full, bx * 64, c1, c2);
+                tma_load_3d(smem + L::OFF_V + bx * L::BOX_KV, &tm_v, kv_full, bx * 64, c1, c2);
             }
         }
         int it = 0;
@@ -191,19 +208,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 // tensor copies first, so their latency overlaps the L / D loads
                 mbar_arrive_expect_tx(&qd_full[st], 2 * L::TILE_Q);
+                const int c1 = p.varlen ? h : q_base, c2 = p.varlen ? row0 + q_base : plane;
                 for (int bx = 0; bx < L::NBOX; ++bx) {
-                    tma_load_3d(q_stage(st) + bx * L::BOX_Q, &tm_q, &qd_full[st], bx * 64, q_base, plane);
-                    tma_load_3d(do_stage(st) + bx * L::BOX_Q, &tm_do, &qd_full[st], bx * 64, q_base, plane);
+                    tma_load_3d(q_stage(st) + bx * L::BOX_Q, &tm_q, &qd_full[st], bx * 64, c1, c2);
+                    tma_load_3d(do_stage(st) + bx * L::BOX_Q, &tm_do, &qd_full[st], bx * 64, c1, c2);
                 }
             }
             float *l2s = ld_smem + st * 2 * kBQ;
             float *dsm = l2s + kBQ;
             for (int r = lane; r < kBQ; r += 32) {
                 const int row = q_base + r;
-                const bool in = row < p.N;
+                const bool in = row < N;
+                const size_t li = p.varlen ? (size_t)h * p.total + row0 + row : (size_t)plane * N + row;
                 // stored negated in log2 units; rows past N get -inf, so P = 0
-                l2s[r] = in ? -p.lse[(size_t)plane * p.N + row] * 1.4426950408889634f : -INFINITY;
-                dsm[r] = in ? p.Dvec[(size_t)plane * p.N + row] : 0.0f;
+                l2s[r] = in ? -p.lse[li] * 1.4426950408889634f : -INFINITY;
+                dsm[r] = in ? p.Dvec[li] : 0.0f;
             }
             mbar_arrive(&qd_full[st]);  // releases this lane's L / D writes
         }
@@ -319,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv = kv0 + c;
         // a key row past N (zero-filled by the copy) must give P = 0: its
         // score 0 is not covered by L, and exp(0 - L) can overflow
-        const bool kv_oob = kv >= p.N;
+        const bool kv_oob = kv >= N;
         bool ok = true;
         for (int it = 0; it < n_it; ++it) {
             const int st = it % QS;
@@ -421,21 +440,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float a1 = __uint_as_float(o[2 * x + 1]) * f;
                     w[x] = BF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
                 }
-                uint8_t *rowp = stage + (c0 >> 6) * L::BOX_KV + c * 128;
+                if (p.varlen) {
+                    // packed rows: a 128-row box past this sequence's end would
+                    // overwrite the next sequence, so each thread stores its row
+                    if (kv < N) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(hf == 0 ? p.dv : p.dk) +
+                                                               ((size_t)(row0 + kv) * p.Hkv + g) * (D * 2));
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = ((c0 & 63) >> 3) + q;
-                    *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (c & 7)) << 4)) =
-                        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                        for (int q = 0; q < 4; ++q)
+                            dst[c0 / 8 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    }
+                } else {
+                    uint8_t *rowp = stage + (c0 >> 6) * L::BOX_KV + c * 128;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int chunk = ((c0 & 63) >> 3) + q;
+                        *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (c & 7)) << 4)) =
+                            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    }
                 }
             }
-            fence_proxy_async_smem();
-            named_bar_sync(1 + hf, 128);
-            if (c == 0) {
-                const CUtensorMap *tm = hf == 0 ? &tm_dv : &tm_dk;
-                for (int bx = 0; bx < L::NBOX; ++bx) tma_store_3d(tm, stage + bx * L::BOX_KV, bx * 64, kv0, bg);
-                bulk_commit();
-                bulk_wait_read_all();
+            if (!p.varlen) {
+                fence_proxy_async_smem();
+                named_bar_sync(1 + hf, 128);
+                if (c == 0) {
+                    const CUtensorMap *tm = hf == 0 ? &tm_dv : &tm_dk;
+                    for (int bx = 0; bx < L::NBOX; ++bx) tma_store_3d(tm, stage + bx * L::BOX_KV, bx * 64, kv0, bg);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
             }
         }
         __syncwarp();
@@ -460,14 +493,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(dq_free);
             const int h = g * G + it / n_i;
             const int q_first = (i_start + it % n_i) * kBQ + hf * 64;
-            const int rows = min(64, p.N - q_first);
+            const int rows = min(64, N - q_first);
             if (t < D) {
                 // element (q, t) of this head's dQ: consecutive lanes touch
                 // consecutive floats (one 128-byte line per warp and row)
-                float *dst = p.dq_acc + ((size_t)(b * p.Hq + h) * p.N + q_first) * D + t;
+                // dense: [B][Hq][N][d]; packed: [total][Hq][d]
+                const size_t rstride = p.varlen ? (size_t)p.Hq * D : (size_t)D;
+                float *dst = p.dq_acc + (p.varlen ? ((size_t)(row0 + q_first) * p.Hq + h) * D
+                                                  : ((size_t)(b * p.Hq + h) * N + q_first) * D) + t;
 #pragma unroll
                 for (int r = 0; r < 64; ++r)
-                    if (r < rows) atomicAdd(dst + (size_t)r * D, __uint_as_float(v[r]));
+                    if (r < rows) atomicAdd(dst + (size_t)r * rstride, __uint_as_float(v[r]));
             }
         }
         __syncwarp();
@@ -482,11 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // D[row] = sum_c dO[row, c] * O[row, c]; also zeroes the fp32 dQ accumulator.
-// 16 lanes per row, 16-byte loads.
+// 16 lanes per row, 16-byte loads.  Rows are taken in memory order; in the
+// packed layout row t * Hq + h is stored at D[h * total + t] (the LSE layout).
 template <bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4 *__restrict__ o, const uint4 *__restrict__ dO,
                                                       float *__restrict__ Dvec, float4 *__restrict__ dq_acc,
-                                                      long rows, int d, long acc_vec4) {
+                                                      long rows, int d, long acc_vec4, int Hq, long total,
+                                                      int varlen) {
     const long tid = (long)blockIdx.x * blockDim.x + threadIdx.x;
     const long nthreads = (long)gridDim.x * blockDim.x;
     const int vec_per_row = d / 8;  // 8 elements per uint4
@@ -516,7 +554,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4 *__restrict__ 
         }
 #pragma unroll
         for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (sub == 0 && row < rows) Dvec[row] = acc;
+        if (sub == 0 && row < rows) Dvec[varlen ? (row % Hq) * total + row / Hq : row] = acc;
     }
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
     for (long i = tid; i < acc_vec4; i += nthreads) dq_acc[i] = z;
@@ -590,7 +628,10 @@ struct DqLayout {
 struct DqParams {
     const float *lse;
     const float *Dvec;
+    void *dq;                // packed layout: stored row by row
     unsigned int *status;
+    const int *cu_seqlens;   // packed layout: sequence b is rows cu[b] .. cu[b+1]-1
+    int varlen, total;
     int Hq, Hkv, N, nq, nkv;
     int causal;
     int window;  // > 0: query r sees keys r - window + 1 .. r only
@@ -635,9 +676,22 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int qt = p.causal ? (p.nq - 1 - qt_lin) : qt_lin;
     const int b = bh / p.Hq;
     const int h = bh - b * p.Hq;
-    const int kv_plane = b * p.Hkv + h / (p.Hq / p.Hkv);
+    const int hk = h / (p.Hq / p.Hkv);
+    const int kv_plane = b * p.Hkv + hk;
     const int q0 = qt * 128;
-    const int j_end = p.causal ? min(qt + 1, p.nkv) : p.nkv;
+    // rows of this sequence (packed layout: rows row0 .. row0 + N - 1)
+    int N = p.N, row0 = 0;
+    if (p.varlen) {
+        row0 = p.cu_seqlens[b];
+        N = p.cu_seqlens[b + 1] - row0;
+        if (N < 0 || N > p.N || row0 < 0 || row0 + N > p.total) {
+            if (threadIdx.x == 0 && qt_lin == 0) record_bad_args(p.status);
+            return;  // uniform across the CTA, nothing started yet
+        }
+    }
+    if (q0 >= N) return;  // Q tile past the end of a shorter sequence
+    const int nkv = (N + 127) / 128;
+    const int j_end = p.causal ? min(qt + 1, nkv) : nkv;
     // sliding window of W keys: the first key any row of this tile sees is
     // q0 - W + 1, so K/V tiles before its tile are skipped
     const int j_lo = p.window > 0 ? max(0, q0 - p.window + 1) / 128 : 0;
@@ -670,8 +724,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             prefetch_tmap(&tm_v);
             mbar_arrive_expect_tx(q_full, 2 * L::TILE);
             for (int bx = 0; bx < L::NBOX; ++bx) {
-                tma_load_3d(smem + L::OFF_Q + bx * L::BOX, &tm_q, q_full, bx * 64, q0, bh);
-                tma_load_3d(smem + L::OFF_DO + bx * L::BOX, &tm_do, q_full, bx * 64, q0, bh);
+                const int c1 = p.varlen ? h : q0, c2 = p.varlen ? row0 + q0 : bh;
+                tma_load_3d(smem + L::OFF_Q + bx * L::BOX, &tm_q, q_full, bx * 64, c1, c2);
+                tma_load_3d(smem + L::OFF_DO + bx * L::BOX, &tm_do, q_full, bx * 64, c1, c2);
             }
             int nk = 0, nv = 0;  // tiles whose copies were issued
             for (int j = 0; j < n_j; ++j) {
@@ -680,14 +735,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 mbar_arrive_expect_tx(&k_full[ks], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_K + ks * L::TILE + bx * L::BOX, &tm_k, &k_full[ks], bx * 64,
-                                (j_lo + j) * 128, kv_plane);
+                                p.varlen ? hk : (j_lo + j) * 128, p.varlen ? row0 + (j_lo + j) * 128 : kv_plane);
                 ++nk;
                 const int vs = j % VS;
                 if (j >= VS && !mbar_wait(&v_empty[vs], ((j / VS) + 1) & 1, abort_flag, p.status, 42)) break;
                 mbar_arrive_expect_tx(&v_full[vs], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_V + vs * L::TILE + bx * L::BOX, &tm_v, &v_full[vs], bx * 64,
-                                (j_lo + j) * 128, kv_plane);
+                                p.varlen ? hk : (j_lo + j) * 128, p.varlen ? row0 + (j_lo + j) * 128 : kv_plane);
                 ++nv;
             }
             if (*abort_flag) {
@@ -775,13 +830,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int r = quarter * 32 + lane;  // query row == TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const int q = q0 + r;
-        const bool q_in = q < p.N;
+        const bool q_in = q < N;
+        const size_t li = p.varlen ? (size_t)h * p.total + row0 + q : (size_t)bh * N + q;
         // rows past N: P = 0 (their dQ rows are not stored)
-        const float nl2 = q_in ? -p.lse[(size_t)bh * p.N + q] * 1.4426950408889634f : -INFINITY;
-        const float dq_d = q_in ? p.Dvec[(size_t)bh * p.N + q] : 0.0f;
+        const float nl2 = q_in ? -p.lse[li] * 1.4426950408889634f : -INFINITY;
+        const float dq_d = q_in ? p.Dvec[li] : 0.0f;
         // keys this row attends to: kv_lo .. kv_last (causal: up to q; never
         // a key past N; sliding window: from q - W + 1)
-        const int kv_last = p.causal ? min(q, p.N - 1) : p.N - 1;
+        const int kv_last = p.causal ? min(q, N - 1) : N - 1;
         const int kv_lo = p.window > 0 ? q - p.window + 1 : 0;
         const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 nl2x2 = make_float2(nl2, nl2);
@@ -854,20 +910,35 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     const float a1 = __uint_as_float(o[2 * x + 1]) * p.scale;
                     w[x] = BF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
                 }
-                uint8_t *rowp = stage + (c0 >> 6) * L::BOX + r * 128;
+                if (p.varlen) {
+                    // packed rows: each thread stores its own row (a 128-row box
+                    // past this sequence's end would overwrite the next one)
+                    if (q_in) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.dq) +
+                                                               ((size_t)(row0 + q) * p.Hq + h) * (D * 2));
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const int chunk = ((c0 & 63) >> 3) + x;
-                    *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (r & 7)) << 4)) =
-                        make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                        for (int x = 0; x < 4; ++x)
+                            dst[c0 / 8 + x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                    }
+                } else {
+                    uint8_t *rowp = stage + (c0 >> 6) * L::BOX + r * 128;
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int chunk = ((c0 & 63) >> 3) + x;
+                        *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (r & 7)) << 4)) =
+                            make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                    }
                 }
             }
-            fence_proxy_async_smem();
-            named_bar_sync(1, kDqSoftmaxThreads);
-            if (threadIdx.x == 0) {
-                for (int bx = 0; bx < L::NBOX; ++bx) tma_store_3d(&tm_dq, stage + bx * L::BOX, bx * 64, q0, bh);
-                bulk_commit();
-                bulk_wait_read_all();
+            if (!p.varlen) {
+                fence_proxy_async_smem();
+                named_bar_sync(1, kDqSoftmaxThreads);
+                if (threadIdx.x == 0) {
+                    for (int bx = 0; bx < L::NBOX; ++bx)
+                        tma_store_3d(&tm_dq, stage + bx * L::BOX, bx * 64, q0, bh);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
             }
         }
         __syncwarp();
@@ -893,23 +964,20 @@ template <int D, bool BF16>
 cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
     using L = BwdLayout<D>;
     const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const uint64_t N = a.N;
-    const uint64_t pq = (uint64_t)a.B * a.Hq, pkv = (uint64_t)a.B * a.Hkv;
+    const SeqLayout &lay = a.lay;
     CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
-    if (!make_tmap_3d(&tq, a.q, dt, 2, D, N, pq, 64, kBQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_3d(&tdo, a.dO, dt, 2, D, N, pq, 64, kBQ, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_3d(&tk, a.k, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_3d(&tv, a.v, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_3d(&tdk, a.dk, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_3d(&tdv, a.dv, dt, 2, D, N, pkv, 64, kBKV, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        (two_pass && !make_tmap_3d(&tdq, a.dq, dt, 2, D, N, pq, 64, kBQ, CU_TENSOR_MAP_SWIZZLE_128B)))
+    if (!make_tmap_tiles(&tq, a.q, dt, D, lay, a.Hq, kBQ) || !make_tmap_tiles(&tdo, a.dO, dt, D, lay, a.Hq, kBQ) ||
+        !make_tmap_tiles(&tk, a.k, dt, D, lay, a.Hkv, kBKV) || !make_tmap_tiles(&tv, a.v, dt, D, lay, a.Hkv, kBKV) ||
+        !make_tmap_tiles(&tdk, a.dk, dt, D, lay, a.Hkv, kBKV) ||
+        !make_tmap_tiles(&tdv, a.dv, dt, D, lay, a.Hkv, kBKV) ||
+        (two_pass && !make_tmap_tiles(&tdq, a.dq, dt, D, lay, a.Hq, kBQ)))
         return cudaErrorInvalidValue;
 
-    const long rows = (long)a.B * a.Hq * a.N;
+    const long rows = (long)lay.total * a.Hq;  // dense: total = B * N
     const int eb = elementwise_blocks();
     bwd_pre_kernel<BF16><<<eb, 256, 0, st>>>(static_cast<const uint4 *>(a.o), static_cast<const uint4 *>(a.dO),
                                              a.D, reinterpret_cast<float4 *>(a.dq_acc), rows, D,
-                                             two_pass ? 0 : rows * D / 4);
+                                             two_pass ? 0 : rows * D / 4, a.Hq, (long)lay.total, lay.varlen);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -920,7 +988,12 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
     p.lse = a.lse;
     p.Dvec = a.D;
     p.dq_acc = a.dq_acc;
+    p.dk = a.dk;
+    p.dv = a.dv;
     p.status = device_status_ptr();
+    p.cu_seqlens = lay.cu_seqlens;
+    p.varlen = lay.varlen;
+    p.total = lay.total;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.N = a.N;
@@ -944,6 +1017,10 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
         pq2.lse = a.lse;
         pq2.Dvec = a.D;
         pq2.status = p.status;
+        pq2.dq = a.dq;
+        pq2.cu_seqlens = lay.cu_seqlens;
+        pq2.varlen = lay.varlen;
+        pq2.total = lay.total;
         pq2.Hq = a.Hq;
         pq2.Hkv = a.Hkv;
         pq2.N = a.N;

@@ -67,9 +67,12 @@ struct FwdLayout {
 };
 
 struct FwdParams {
+    void *o;
     float *lse;
     unsigned int *status;
-    int Hq, Hkv, N, nblk, causal;  // nblk: 256-row blocks per head
+    const int *cu_seqlens;         // packed layout: sequence b is rows cu[b] .. cu[b+1]-1
+    int varlen, total;             // packed layout flag, rows of all sequences
+    int Hq, Hkv, N, nblk, causal;  // N: rows per sequence (packed: the maximum); nblk: 256-row blocks
     int window;                    // > 0: row r sees keys r - window + 1 .. r only
     float scale_log2;              // scale * log2(e)
 };
@@ -109,10 +112,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = bh - b * p.Hq;
     const int hk = h / (p.Hq / p.Hkv);
     const int q0a = t * 2 * kBM;
-    const int nkv_all = (p.N + kBN - 1) / kBN;
+    // rows of this sequence: N of them; packed sequences start at row0 of the
+    // token-major tensors ("variable length sequence" of the FA3 summary)
+    int N = p.N, row0 = 0;
+    if (p.varlen) {
+        row0 = p.cu_seqlens[b];
+        N = p.cu_seqlens[b + 1] - row0;
+        if (N < 0 || N > p.N || row0 < 0 || row0 + N > p.total) {
+            if (threadIdx.x == 0 && t_lin == 0) record_bad_args(p.status);
+            return;  // uniform across the CTA, nothing started yet
+        }
+    }
+    if (q0a >= N) return;  // block past the end of a shorter sequence
+    const int nkv_all = (N + kBN - 1) / kBN;
     // K/V tiles each Q tile visits; 0 for a tile that lies entirely past N
     const int nA = p.causal ? min(q0a / kBN + 1, nkv_all) : nkv_all;
-    const int nB = q0a + kBM >= p.N ? 0 : (p.causal ? min((q0a + kBM) / kBN + 1, nkv_all) : nkv_all);
+    const int nB = q0a + kBM >= N ? 0 : (p.causal ? min((q0a + kBM) / kBN + 1, nkv_all) : nkv_all);
     const int nmax = max(nA, nB);
     // first K/V tile each Q tile visits: with a sliding window of W keys, row
     // r sees keys r - W + 1 .. r, so tile X starts at the tile holding key
@@ -155,8 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(q_full, ntq * L::TILE);
             for (int x = 0; x < ntq; ++x)
                 for (int bx = 0; bx < L::NBOX; ++bx)
-                    tma_load_3d(smem + L::OFF_Q + x * L::TILE + bx * L::BOX, &tm_q, q_full, bx * 64, q0a + x * kBM,
-                                q_plane);
+                    tma_load_3d(smem + L::OFF_Q + x * L::TILE + bx * L::BOX, &tm_q, q_full, bx * 64,
+                                p.varlen ? h : q0a + x * kBM, p.varlen ? row0 + q0a + x * kBM : q_plane);
             // K_j then V_j: the order in which the MMAs first need them
             int nk = 0, nv = 0;
             for (int j = jA0; j < nmax; ++j) {
@@ -165,15 +180,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u >= L::KS && !mbar_wait(&k_empty[ks], ((u / L::KS) + 1) & 1, abort_flag, p.status, 1)) break;
                 mbar_arrive_expect_tx(&k_full[ks], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
-                    tma_load_3d(smem + L::OFF_K + ks * L::TILE + bx * L::BOX, &tm_k, &k_full[ks], bx * 64, j * kBN,
-                                kv_plane);
+                    tma_load_3d(smem + L::OFF_K + ks * L::TILE + bx * L::BOX, &tm_k, &k_full[ks], bx * 64,
+                                p.varlen ? hk : j * kBN, p.varlen ? row0 + j * kBN : kv_plane);
                 ++nk;
                 const int vs = u % L::VS;
                 if (u >= L::VS && !mbar_wait(&v_empty[vs], ((u / L::VS) + 1) & 1, abort_flag, p.status, 2)) break;
                 mbar_arrive_expect_tx(&v_full[vs], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
-                    tma_load_3d(smem + L::OFF_V + vs * L::TILE + bx * L::BOX, &tm_v, &v_full[vs], bx * 64, j * kBN,
-                                kv_plane);
+                    tma_load_3d(smem + L::OFF_V + vs * L::TILE + bx * L::BOX, &tm_v, &v_full[vs], bx * 64,
+                                p.varlen ? hk : j * kBN, p.varlen ? row0 + j * kBN : kv_plane);
                 ++nv;
             }
             if (*abort_flag) {
@@ -303,11 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait_x32(s + 96);
 
             const int kv0 = j * kBN;
-            const bool need_mask = (kv0 + kBN > p.N) || (p.causal && kv0 + kBN - 1 > q0) ||
+            const bool need_mask = (kv0 + kBN > N) || (p.causal && kv0 + kBN - 1 > q0) ||
                                    (p.window > 0 && kv0 < q0 + kBM - p.window);
             if (need_mask) {
                 // visible: lo <= key < hi
-                const int hi = p.causal ? min(p.N, q0 + row + 1) : p.N;
+                const int hi = p.causal ? min(N, q0 + row + 1) : N;
                 const int lo = p.window > 0 ? q0 + row - p.window + 1 : 0;
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
@@ -417,23 +432,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float bb = __uint_as_float(o[2 * c + 1]) * inv_l;
                         w[c] = BF16 ? pack_bf16x2(a, bb) : pack_f16x2(a, bb);
                     }
-                    uint8_t *rowp = stage + (c0 >> 6) * L::BOX + row * 128;
+                    if (p.varlen) {
+                        // packed rows: a 128-row box past this sequence's end
+                        // would overwrite the next sequence, so each thread
+                        // stores its own row (16-byte stores)
+                        if (q0 + row < N) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.o) +
+                                                                   ((size_t)(row0 + q0 + row) * p.Hq + h) * (D * 2));
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int chunk = ((c0 & 63) >> 3) + q;
-                        *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (row & 7)) << 4)) =
-                            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                            for (int q = 0; q < 4; ++q)
+                                dst[c0 / 8 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                        }
+                    } else {
+                        uint8_t *rowp = stage + (c0 >> 6) * L::BOX + row * 128;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int chunk = ((c0 & 63) >> 3) + q;
+                            *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (row & 7)) << 4)) =
+                                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                        }
                     }
                 }
-                fence_proxy_async_smem();
-                named_bar_sync(1 + x, kBM);
-                if (row == 0) {
-                    for (int bx = 0; bx < L::NBOX; ++bx) tma_store_3d(&tm_o, stage + bx * L::BOX, bx * 64, q0, q_plane);
-                    bulk_commit();
-                    bulk_wait_read_all();
+                if (!p.varlen) {
+                    fence_proxy_async_smem();
+                    named_bar_sync(1 + x, kBM);
+                    if (row == 0) {
+                        for (int bx = 0; bx < L::NBOX; ++bx)
+                            tma_store_3d(&tm_o, stage + bx * L::BOX, bx * 64, q0, q_plane);
+                        bulk_commit();
+                        bulk_wait_read_all();
+                    }
                 }
-                if (q0 + row < p.N)
-                    p.lse[(size_t)q_plane * p.N + q0 + row] = (m_ref + log2f(l_exact)) * 0.69314718055994530942f;
+                if (q0 + row < N) {
+                    const size_t li = p.varlen ? (size_t)h * p.total + row0 + q0 + row : (size_t)q_plane * N + q0 + row;
+                    p.lse[li] = (m_ref + log2f(l_exact)) * 0.69314718055994530942f;
+                }
             }
         }
         __syncwarp();
@@ -452,18 +485,19 @@ cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t st) {
     using L = FwdLayout<D>;
     const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tq, tk, tv, to;
-    const uint64_t N = a.N;
-    if (!make_tmap_3d(&tq, a.q, dt, 2, D, N, (uint64_t)a.B * a.Hq, 64, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_3d(&tk, a.k, dt, 2, D, N, (uint64_t)a.B * a.Hkv, 64, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_3d(&tv, a.v, dt, 2, D, N, (uint64_t)a.B * a.Hkv, 64, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_3d(&to, a.o, dt, 2, D, N, (uint64_t)a.B * a.Hq, 64, kBM, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_tmap_tiles(&tq, a.q, dt, D, a.lay, a.Hq, kBM) || !make_tmap_tiles(&tk, a.k, dt, D, a.lay, a.Hkv, kBN) ||
+        !make_tmap_tiles(&tv, a.v, dt, D, a.lay, a.Hkv, kBN) || !make_tmap_tiles(&to, a.o, dt, D, a.lay, a.Hq, kBM))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::ALLOC);
     if (e != cudaSuccess) return e;
     FwdParams p;
+    p.o = a.o;
     p.lse = a.lse;
     p.status = device_status_ptr();
+    p.cu_seqlens = a.lay.cu_seqlens;
+    p.varlen = a.lay.varlen;
+    p.total = a.lay.total;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.N = a.N;

@@ -16,6 +16,30 @@ bool make_tmap_3d(CUtensorMap *map, const void *base, CUtensorMapDataType dtype,
                   uint64_t dim0, uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1,
                   CUtensorMapSwizzle swizzle);
 
+// Row layout of the sequences of one call.
+//   dense  (varlen = 0): B sequences of N rows; a tensor with H heads is
+//                        [B][H][N][d] and LSE / D are [B][H][N].
+//   packed (varlen = 1): B sequences of cu_seqlens[b+1] - cu_seqlens[b] rows
+//                        (at most N = max_seqlen) stored back to back,
+//                        token-major: [total][H][d]; LSE / D are [H][total].
+struct SeqLayout {
+    int varlen;
+    int B, N;               // sequences, rows per sequence (varlen: the maximum)
+    int total;              // varlen: rows of all sequences (cu_seqlens[B])
+    const int *cu_seqlens;  // varlen: device [B + 1] prefix sums of the lengths
+};
+
+// 3-D tiled TMA descriptor with an explicit three-dimensional box.
+bool make_tmap_3d_box(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int elem_bytes,
+                      uint64_t dim0, uint64_t dim1, uint64_t dim2, uint32_t box0, uint32_t box1, uint32_t box2,
+                      CUtensorMapSwizzle swizzle);
+
+// TMA descriptor for 64-column x `rows`-row boxes of the 16-bit tensor with
+// `heads` heads in layout `lay` (128-byte swizzle).  Dense: coordinates
+// (column, row, plane); packed: (column, head, token).
+bool make_tmap_tiles(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int d, const SeqLayout &lay,
+                     int heads, uint32_t rows);
+
 // Device address of this library's status word on the current device.
 unsigned int *device_status_ptr();
 
@@ -27,6 +51,7 @@ struct FwdArgs {
     float scale;
     bool bf16;
     int window;  // 0: none; > 0: causal sliding window of that many keys
+    SeqLayout lay;
 };
 
 struct BwdArgs {
@@ -37,7 +62,8 @@ struct BwdArgs {
     float scale;
     bool bf16;
     int window;    // 0: none; > 0: causal sliding window of that many keys
-    float *D;      // [B][Hq][N]
+    SeqLayout lay;
+    float *D;      // [B][Hq][N] (packed: [Hq][total])
     float *dq_acc; // [B][Hq][N][d]; unused (may be null) by the two-pass backward
 };
 

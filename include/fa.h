@@ -159,6 +159,50 @@ fa_status_t fa_bwd_local(const void *q, const void *k, const void *v,
                          size_t workspace_bytes, void *stream);
 
 /*
+ * Forward over a batch of sequences of different lengths packed back to back
+ * ("variable length sequence", named among the optimisations of [FA3]):
+ * sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1 of the packed
+ * tensors and attends only within itself, with the fa_fwd algorithm (causal
+ * and sliding-window masks relative to the sequence start).
+ *   q, o  [total][Hq][d], k, v [total][Hkv][d] (token-major, d contiguous)
+ *   lse   [Hq][total] fp32 (natural log)
+ *   cu_seqlens: DEVICE int32 [B + 1], cu_seqlens[0] = 0, non-decreasing,
+ *   cu_seqlens[B] = total, every length <= max_seqlen (4-byte aligned).
+ *   window: 0 = none, else >= 1 with causal = 1 (as fa_fwd_local).
+ * The offsets are read on the device: lengths that break the rules above are
+ * reported by fa_get_device_status as FA_ERR_INVALID_ARG and the affected
+ * sequences are left unwritten.
+ */
+fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o,
+                          float *lse, const int *cu_seqlens, int B,
+                          int max_seqlen, int total, int Hq, int Hkv, int d,
+                          int causal, int window, float scale,
+                          fa_dtype_t dtype, void *stream);
+
+/*
+ * Workspace of fa_bwd_varlen: D ([Hq][total] fp32, rounded up to 256 bytes)
+ * and, unless deterministic, the fp32 dQ accumulator ([total][Hq][d]).
+ */
+size_t fa_bwd_varlen_workspace_bytes(int total, int Hq, int d,
+                                     int deterministic);
+
+/*
+ * Backward of fa_fwd_varlen: fa_bwd (deterministic = 0, atomic dQ) or
+ * fa_bwd_two_pass (deterministic = 1) on the packed layout above.
+ *   dq [total][Hq][d], dk, dv [total][Hkv][d] (out); other arguments as
+ *   fa_fwd_varlen and fa_bwd; workspace of at least
+ *   fa_bwd_varlen_workspace_bytes(total, Hq, d, deterministic) bytes,
+ *   256-byte aligned.
+ */
+fa_status_t fa_bwd_varlen(const void *q, const void *k, const void *v,
+                          const void *o, const float *lse, const void *dO,
+                          void *dq, void *dk, void *dv, const int *cu_seqlens,
+                          int B, int max_seqlen, int total, int Hq, int Hkv,
+                          int d, int causal, int window, float scale,
+                          fa_dtype_t dtype, int deterministic, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/*
  * Size of the scratch buffer built into the library for fa_bwd_noalloc:
  * 64 MiB per device.
  */
