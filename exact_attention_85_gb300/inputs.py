@@ -110,3 +110,32 @@ def make_custom(B, Hq, Hkv, N, d, dtype=torch.bfloat16, seed=0, with_grad=True):
     if with_grad:
         out["dO"] = torch.randn(B, Hq, N, d, generator=g).to(dtype)
     return out
+
+
+def varlen_lengths(B: int, max_len: int, seed: int = 0) -> list[int]:
+    """A seeded length mix for a packed batch: B lengths drawn uniformly
+    from 1 .. max_len (the pages name variable-length batches but give no
+    length distribution; tests add the edge lengths explicitly)."""
+    g = torch.Generator().manual_seed(seed)
+    return [int(x) for x in torch.randint(1, max_len + 1, (B,), generator=g)]
+
+
+def make_varlen(lengths, Hq: int, Hkv: int, d: int, dtype=torch.bfloat16, seed: int = 0,
+                with_grad: bool = True) -> dict:
+    """Packed token-major tensors for sequences of the given lengths:
+    q [total, Hq, d], k, v [total, Hkv, d], dO [total, Hq, d] drawn N(0, 1)
+    in that order (then cast), and cu_seqlens int32 [B + 1] (prefix sums)."""
+    g = torch.Generator().manual_seed(seed)
+    total = int(sum(lengths))
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    out = {
+        "q": torch.randn(total, Hq, d, generator=g).to(dtype),
+        "k": torch.randn(total, Hkv, d, generator=g).to(dtype),
+        "v": torch.randn(total, Hkv, d, generator=g).to(dtype),
+        "cu_seqlens": torch.tensor(cu, dtype=torch.int32),
+    }
+    if with_grad:
+        out["dO"] = torch.randn(total, Hq, d, generator=g).to(dtype)
+    return out

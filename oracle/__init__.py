@@ -210,3 +210,40 @@ def fp8_reference(q, k, v, signs, causal: bool, scale: float):
     unpinned by the pages, which report only a 2.6x ratio.
     """
     return attention_fwd(*fp8_dequantized(q, k, v, signs), causal, scale)
+
+
+def _segments(cu):
+    cu = [int(x) for x in (cu.tolist() if hasattr(cu, "tolist") else cu)]
+    return [(cu[i], cu[i + 1]) for i in range(len(cu) - 1)]
+
+
+def attention_fwd_varlen(q, k, v, cu_seqlens, causal: bool, scale: float, window: int = 0):
+    """Packed sequences (token-major q [total,Hq,d], k/v [total,Hkv,d]):
+    every sequence attends only within itself, so this is attention_fwd on
+    each sequence in turn.  Returns O [total,Hq,d] and L [Hq,total]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    total, Hq, d = q.shape
+    o = np.zeros_like(q)
+    lse = np.zeros((Hq, total), dtype=np.float64)
+    for a, b in _segments(cu_seqlens):
+        if b == a:
+            continue
+        ob, lb = attention_fwd(q[a:b].transpose(1, 0, 2)[None], k[a:b].transpose(1, 0, 2)[None],
+                               v[a:b].transpose(1, 0, 2)[None], causal, scale, window)
+        o[a:b] = ob[0].transpose(1, 0, 2)
+        lse[:, a:b] = lb[0]
+    return o, lse
+
+
+def attention_bwd_varlen(q, k, v, dO, cu_seqlens, causal: bool, scale: float, window: int = 0):
+    """Gradients for packed sequences: attention_bwd on each sequence in turn.
+    Returns dQ [total,Hq,d], dK, dV [total,Hkv,d]."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for a, b in _segments(cu_seqlens):
+        if b == a:
+            continue
+        t = lambda x: x[a:b].transpose(1, 0, 2)[None]  # noqa: E731
+        gq, gk, gv = attention_bwd(t(q), t(k), t(v), t(dO), causal, scale, window)
+        dq[a:b], dk[a:b], dv[a:b] = (g[0].transpose(1, 0, 2) for g in (gq, gk, gv))
+    return dq, dk, dv

@@ -434,3 +434,42 @@ def test_window_at_least_n_is_plain_causal():
         a = oracle.attention_fwd(q, k, v, True, 0.3, window=w)
         b = oracle.attention_fwd(q, k, v, True, 0.3)
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ------------------------------------------------- packed variable lengths
+
+
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (True, 3)])
+def test_varlen_matches_block_diagonal_sdpa(causal, window):
+    """Packed sequences attend only within themselves: torch SDPA on the
+    whole packed batch with a block-diagonal (and causal / window) mask is the
+    independent reference, forward and backward.  Includes an empty sequence
+    and one of a single row."""
+    lengths = [5, 0, 1, 9, 4]
+    Hq, Hkv, d = 4, 2, 8
+    total = sum(lengths)
+    q, k, v, dO = (_rand((total, h, d), s) for h, s in ((Hq, 41), (Hkv, 42), (Hkv, 43), (Hq, 44)))
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    scale = 0.5
+    o, lse = oracle.attention_fwd_varlen(q, k, v, cu, causal, scale, window)
+    dq, dk, dv = oracle.attention_bwd_varlen(q, k, v, dO, cu, causal, scale, window)
+    seq = np.repeat(np.arange(len(lengths)), lengths)
+    pos = np.concatenate([np.arange(n) for n in lengths])
+    mask = seq[:, None] == seq[None, :]
+    if causal:
+        mask &= pos[None, :] <= pos[:, None]
+    if window:
+        mask &= pos[:, None] - pos[None, :] < window
+    G = Hq // Hkv
+    qt, kt, vt = (torch.tensor(x.transpose(1, 0, 2)[None].copy(), requires_grad=True) for x in (q, k, v))
+    ot = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt.repeat_interleave(G, 1), vt.repeat_interleave(G, 1), attn_mask=torch.tensor(mask), scale=scale)
+    ot.backward(torch.tensor(dO.transpose(1, 0, 2)[None].copy()))
+    np.testing.assert_allclose(o, ot.detach().numpy()[0].transpose(1, 0, 2), atol=1e-12)
+    np.testing.assert_allclose(dq, qt.grad.numpy()[0].transpose(1, 0, 2), atol=1e-11)
+    np.testing.assert_allclose(dk, kt.grad.numpy()[0].transpose(1, 0, 2), atol=1e-11)
+    np.testing.assert_allclose(dv, vt.grad.numpy()[0].transpose(1, 0, 2), atol=1e-11)
+    from scipy.special import logsumexp
+    for h in range(Hq):
+        s = np.where(mask, scale * q[:, h] @ k[:, h // G].T, -np.inf)
+        np.testing.assert_allclose(lse[h], logsumexp(s, axis=1), atol=1e-12)
