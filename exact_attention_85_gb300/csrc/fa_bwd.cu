@@ -95,7 +95,8 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 128, kColDV = 256, kColDK =
 
 // DQ = false builds the first pass of the deterministic two-pass backward:
 // only dK and dV, no dQ^T MMA, no dS in shared memory, no atomics.
-template <int D, bool BF16, bool DQ>
+// GENERAL = false compiles the sliding window and the packed layout out.
+template <int D, bool BF16, bool DQ, bool GENERAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -126,6 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int win = GENERAL ? p.window : 0;
+    const bool packed = GENERAL && p.varlen;
 
     const int bg = blockIdx.x / p.nkv;  // batch * Hkv + g
     const int jt = blockIdx.x - bg * p.nkv;
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows of this sequence (packed layout: rows row0 .. row0 + N - 1 of the
     // token-major tensors)
     int N = p.N, row0 = 0;
-    if (p.varlen) {
+    if (packed) {
         row0 = p.cu_seqlens[b];
         N = p.cu_seqlens[b + 1] - row0;
         if (N < 0 || N > p.N || row0 < 0 || row0 + N > p.total) {
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i_start = p.causal ? jt : 0;  // first Q tile with a row >= kv0 (equal tile sizes)
     // with a sliding window of W keys the last query row that sees any key of
     // this tile is kv0 + 127 + W - 1; later Q tiles are skipped
-    const int i_end = p.window > 0 ? min(nq, (kv0 + kBKV + p.window - 2) / kBQ + 1) : nq;
+    const int i_end = win > 0 ? min(nq, (kv0 + kBKV + win - 2) / kBQ + 1) : nq;
     const int n_i = i_end - i_start;
     const int n_it = G * n_i;
 
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_do);
             mbar_arrive_expect_tx(kv_full, 2 * L::TILE_KV);
             for (int bx = 0; bx < L::NBOX; ++bx) {
-                const int c1 = p.varlen ? g : kv0, c2 = p.varlen ? row0 + kv0 : bg;
+                const int c1 = packed ? g : kv0, c2 = packed ? row0 + kv0 : bg;
                 tma_load_3d(smem + L::OFF_K + bx * L::BOX_KV, &tm_k, kv_full, bx * 64, c1, c2);
                 tma_load_3d(smem + L::OFF_V + bx * L::BOX_KV, &tm_v, kv_full, bx * 64, c1, c2);
             }
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 // tensor copies first, so their latency overlaps the L / D loads
                 mbar_arrive_expect_tx(&qd_full[st], 2 * L::TILE_Q);
-                const int c1 = p.varlen ? h : q_base, c2 = p.varlen ? row0 + q_base : plane;
+                const int c1 = packed ? h : q_base, c2 = packed ? row0 + q_base : plane;
                 for (int bx = 0; bx < L::NBOX; ++bx) {
                     tma_load_3d(q_stage(st) + bx * L::BOX_Q, &tm_q, &qd_full[st], bx * 64, c1, c2);
                     tma_load_3d(do_stage(st) + bx * L::BOX_Q, &tm_do, &qd_full[st], bx * 64, c1, c2);
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int r = lane; r < kBQ; r += 32) {
                 const int row = q_base + r;
                 const bool in = row < N;
-                const size_t li = p.varlen ? (size_t)h * p.total + row0 + row : (size_t)plane * N + row;
+                const size_t li = packed ? (size_t)h * p.total + row0 + row : (size_t)plane * N + row;
                 // stored negated in log2 units; rows past N get -inf, so P = 0
                 l2s[r] = in ? -p.lse[li] * 1.4426950408889634f : -INFINITY;
                 dsm[r] = in ? p.Dvec[li] : 0.0f;
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int q_base = (i_start + it % n_i) * kBQ;
             const bool diag = p.causal && (q_base + hf * 64 < kv0 + kBKV);
             // some query of this half is W or more rows below some key of the tile
-            const bool wmask = p.window > 0 && (q_base + hf * 64 + 63 - kv0 >= p.window);
+            const bool wmask = win > 0 && (q_base + hf * 64 + 63 - kv0 >= win);
             uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
@@ -376,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (kv > q_first + r + 1) p1 = 0.0f;
                     }
                     if (wmask) {  // sliding window: visible iff q - kv < W
-                        if (q_first + r - kv >= p.window) p0 = 0.0f;
-                        if (q_first + r + 1 - kv >= p.window) p1 = 0.0f;
+                        if (q_first + r - kv >= win) p0 = 0.0f;
+                        if (q_first + r + 1 - kv >= win) p1 = 0.0f;
                     }
                     const float2 t = fsub2(make_float2(__uint_as_float(dp[r]), __uint_as_float(dp[r + 1])),
                                            *reinterpret_cast<const float2 *>(dsm + r));
@@ -440,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float a1 = __uint_as_float(o[2 * x + 1]) * f;
                     w[x] = BF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
                 }
-                if (p.varlen) {
+                if (packed) {
                     // packed rows: a 128-row box past this sequence's end would
                     // overwrite the next sequence, so each thread stores its row
                     if (kv < N) {
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (!p.varlen) {
+            if (!packed) {
                 fence_proxy_async_smem();
                 named_bar_sync(1 + hf, 128);
                 if (c == 0) {
@@ -497,13 +500,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t < D) {
                 // element (q, t) of this head's dQ: consecutive lanes touch
                 // consecutive floats (one 128-byte line per warp and row)
-                // dense: [B][Hq][N][d]; packed: [total][Hq][d]
-                const size_t rstride = p.varlen ? (size_t)p.Hq * D : (size_t)D;
-                float *dst = p.dq_acc + (p.varlen ? ((size_t)(row0 + q_first) * p.Hq + h) * D
-                                                  : ((size_t)(b * p.Hq + h) * N + q_first) * D) + t;
+                if (packed) {  // packed: [total][Hq][d]
+                    float *dst = p.dq_acc + ((size_t)(row0 + q_first) * p.Hq + h) * D + t;
+                    const size_t rstride = (size_t)p.Hq * D;
 #pragma unroll
-                for (int r = 0; r < 64; ++r)
-                    if (r < rows) atomicAdd(dst + (size_t)r * rstride, __uint_as_float(v[r]));
+                    for (int r = 0; r < 64; ++r)
+                        if (r < rows) atomicAdd(dst + (size_t)r * rstride, __uint_as_float(v[r]));
+                } else {  // dense: [B][Hq][N][d], constant row stride
+                    float *dst = p.dq_acc + ((size_t)(b * p.Hq + h) * N + q_first) * D + t;
+#pragma unroll
+                    for (int r = 0; r < 64; ++r)
+                        if (r < rows) atomicAdd(dst + (size_t)r * D, __uint_as_float(v[r]));
+                }
             }
         }
         __syncwarp();
@@ -638,7 +646,7 @@ struct DqParams {
     float scale, scale_log2;
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool GENERAL>
 __global__ void __launch_bounds__(kDqThreads, 1)
     bwd_dq_pass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -668,6 +676,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int win = GENERAL ? p.window : 0;
+    const bool packed = GENERAL && p.varlen;
 
     // consecutive CTAs share a head (its K/V stay in L2); causal tiles go
     // longest first within a head
@@ -681,7 +691,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int q0 = qt * 128;
     // rows of this sequence (packed layout: rows row0 .. row0 + N - 1)
     int N = p.N, row0 = 0;
-    if (p.varlen) {
+    if (packed) {
         row0 = p.cu_seqlens[b];
         N = p.cu_seqlens[b + 1] - row0;
         if (N < 0 || N > p.N || row0 < 0 || row0 + N > p.total) {
@@ -694,7 +704,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int j_end = p.causal ? min(qt + 1, nkv) : nkv;
     // sliding window of W keys: the first key any row of this tile sees is
     // q0 - W + 1, so K/V tiles before its tile are skipped
-    const int j_lo = p.window > 0 ? max(0, q0 - p.window + 1) / 128 : 0;
+    const int j_lo = win > 0 ? max(0, q0 - win + 1) / 128 : 0;
     const int n_j = j_end - j_lo;  // K/V tiles j_lo .. j_end - 1, counted from 0 below
 
     if (threadIdx.x == 0) {
@@ -724,7 +734,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             prefetch_tmap(&tm_v);
             mbar_arrive_expect_tx(q_full, 2 * L::TILE);
             for (int bx = 0; bx < L::NBOX; ++bx) {
-                const int c1 = p.varlen ? h : q0, c2 = p.varlen ? row0 + q0 : bh;
+                const int c1 = packed ? h : q0, c2 = packed ? row0 + q0 : bh;
                 tma_load_3d(smem + L::OFF_Q + bx * L::BOX, &tm_q, q_full, bx * 64, c1, c2);
                 tma_load_3d(smem + L::OFF_DO + bx * L::BOX, &tm_do, q_full, bx * 64, c1, c2);
             }
@@ -735,14 +745,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 mbar_arrive_expect_tx(&k_full[ks], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_K + ks * L::TILE + bx * L::BOX, &tm_k, &k_full[ks], bx * 64,
-                                p.varlen ? hk : (j_lo + j) * 128, p.varlen ? row0 + (j_lo + j) * 128 : kv_plane);
+                                packed ? hk : (j_lo + j) * 128, packed ? row0 + (j_lo + j) * 128 : kv_plane);
                 ++nk;
                 const int vs = j % VS;
                 if (j >= VS && !mbar_wait(&v_empty[vs], ((j / VS) + 1) & 1, abort_flag, p.status, 42)) break;
                 mbar_arrive_expect_tx(&v_full[vs], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_V + vs * L::TILE + bx * L::BOX, &tm_v, &v_full[vs], bx * 64,
-                                p.varlen ? hk : (j_lo + j) * 128, p.varlen ? row0 + (j_lo + j) * 128 : kv_plane);
+                                packed ? hk : (j_lo + j) * 128, packed ? row0 + (j_lo + j) * 128 : kv_plane);
                 ++nv;
             }
             if (*abort_flag) {
@@ -831,14 +841,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         const int q = q0 + r;
         const bool q_in = q < N;
-        const size_t li = p.varlen ? (size_t)h * p.total + row0 + q : (size_t)bh * N + q;
+        const size_t li = packed ? (size_t)h * p.total + row0 + q : (size_t)bh * N + q;
         // rows past N: P = 0 (their dQ rows are not stored)
         const float nl2 = q_in ? -p.lse[li] * 1.4426950408889634f : -INFINITY;
         const float dq_d = q_in ? p.Dvec[li] : 0.0f;
         // keys this row attends to: kv_lo .. kv_last (causal: up to q; never
         // a key past N; sliding window: from q - W + 1)
         const int kv_last = p.causal ? min(q, N - 1) : N - 1;
-        const int kv_lo = p.window > 0 ? q - p.window + 1 : 0;
+        const int kv_lo = win > 0 ? q - win + 1 : 0;
         const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 nl2x2 = make_float2(nl2, nl2);
         const float2 dx2 = make_float2(dq_d, dq_d);
@@ -910,7 +920,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     const float a1 = __uint_as_float(o[2 * x + 1]) * p.scale;
                     w[x] = BF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
                 }
-                if (p.varlen) {
+                if (packed) {
                     // packed rows: each thread stores its own row (a 128-row box
                     // past this sequence's end would overwrite the next one)
                     if (q_in) {
@@ -930,7 +940,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     }
                 }
             }
-            if (!p.varlen) {
+            if (!packed) {
                 fence_proxy_async_smem();
                 named_bar_sync(1, kDqSoftmaxThreads);
                 if (threadIdx.x == 0) {
@@ -981,7 +991,9 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
-    auto main_kernel = two_pass ? bwd_main_kernel<D, BF16, false> : bwd_main_kernel<D, BF16, true>;
+    const bool general = a.window > 0 || lay.varlen;
+    auto main_kernel = two_pass ? (general ? bwd_main_kernel<D, BF16, false, true> : bwd_main_kernel<D, BF16, false, false>)
+                                : (general ? bwd_main_kernel<D, BF16, true, true> : bwd_main_kernel<D, BF16, true, false>);
     e = cudaFuncSetAttribute(main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     BwdParams p;
@@ -1010,8 +1022,8 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
 
     if (two_pass) {
         using LQ = DqLayout<D>;
-        e = cudaFuncSetAttribute(bwd_dq_pass_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 LQ::ALLOC);
+        auto dq_kernel = general ? bwd_dq_pass_kernel<D, BF16, true> : bwd_dq_pass_kernel<D, BF16, false>;
+        e = cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, LQ::ALLOC);
         if (e != cudaSuccess) return e;
         DqParams pq2;
         pq2.lse = a.lse;
@@ -1031,8 +1043,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
         pq2.scale = a.scale;
         pq2.scale_log2 = p.scale_log2;
         const long long grid2 = (long long)p.nq * a.B * a.Hq;
-        bwd_dq_pass_kernel<D, BF16><<<dim3((unsigned)grid2), dim3(kDqThreads), LQ::ALLOC, st>>>(tq, tk, tv, tdo,
-                                                                                                 tdq, pq2);
+        dq_kernel<<<dim3((unsigned)grid2), dim3(kDqThreads), LQ::ALLOC, st>>>(tq, tk, tv, tdo, tdq, pq2);
         return cudaGetLastError();
     }
 

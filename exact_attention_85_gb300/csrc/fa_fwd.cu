@@ -79,7 +79,9 @@ struct FwdParams {
 
 constexpr uint32_t kColS = 0, kColO = 256;  // + 128 per tile
 
-template <int D, bool BF16>
+// GENERAL = false compiles the sliding window and the packed layout out:
+// the dense, full-causal path keeps the leanest issue and softmax loops.
+template <int D, bool BF16, bool GENERAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -102,6 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int win = GENERAL ? p.window : 0;
+    const bool packed = GENERAL && p.varlen;
 
     // Block schedule: consecutive CTAs share a head (K/V stay hot in L2);
     // within a head, causal blocks go longest first.
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows of this sequence: N of them; packed sequences start at row0 of the
     // token-major tensors ("variable length sequence" of the FA3 summary)
     int N = p.N, row0 = 0;
-    if (p.varlen) {
+    if (packed) {
         row0 = p.cu_seqlens[b];
         N = p.cu_seqlens[b + 1] - row0;
         if (N < 0 || N > p.N || row0 < 0 || row0 + N > p.total) {
@@ -133,8 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // r sees keys r - W + 1 .. r, so tile X starts at the tile holding key
     // q0_X - W + 1 (the tiles before it are skipped like those above the
     // causal diagonal)
-    const int jA0 = p.window > 0 ? max(0, q0a - p.window + 1) / kBN : 0;
-    const int jB0 = p.window > 0 ? max(0, q0a + kBM - p.window + 1) / kBN : 0;
+    const int jA0 = win > 0 ? max(0, q0a - win + 1) / kBN : 0;
+    const int jB0 = win > 0 ? max(0, q0a + kBM - win + 1) / kBN : 0;
     const int kv_plane = b * p.Hkv + hk;
     const int q_plane = b * p.Hq + h;
 
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int x = 0; x < ntq; ++x)
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_Q + x * L::TILE + bx * L::BOX, &tm_q, q_full, bx * 64,
-                                p.varlen ? h : q0a + x * kBM, p.varlen ? row0 + q0a + x * kBM : q_plane);
+                                packed ? h : q0a + x * kBM, packed ? row0 + q0a + x * kBM : q_plane);
             // K_j then V_j: the order in which the MMAs first need them
             int nk = 0, nv = 0;
             for (int j = jA0; j < nmax; ++j) {
@@ -181,14 +185,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(&k_full[ks], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_K + ks * L::TILE + bx * L::BOX, &tm_k, &k_full[ks], bx * 64,
-                                p.varlen ? hk : j * kBN, p.varlen ? row0 + j * kBN : kv_plane);
+                                packed ? hk : j * kBN, packed ? row0 + j * kBN : kv_plane);
                 ++nk;
                 const int vs = u % L::VS;
                 if (u >= L::VS && !mbar_wait(&v_empty[vs], ((u / L::VS) + 1) & 1, abort_flag, p.status, 2)) break;
                 mbar_arrive_expect_tx(&v_full[vs], L::TILE);
                 for (int bx = 0; bx < L::NBOX; ++bx)
                     tma_load_3d(smem + L::OFF_V + vs * L::TILE + bx * L::BOX, &tm_v, &v_full[vs], bx * 64,
-                                p.varlen ? hk : j * kBN, p.varlen ? row0 + j * kBN : kv_plane);
+                                packed ? hk : j * kBN, packed ? row0 + j * kBN : kv_plane);
                 ++nv;
             }
             if (*abort_flag) {
@@ -256,27 +260,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nB > 0 && jB0 == jA0) issue_s(1, 0);
                 mma_commit(&k_empty[0]);
             }
-            for (int j = jA0; ok && j < nmax; ++j) {
-                const int u = j - jA0;
-                if (!mbar_wait(&v_full[u % L::VS], (u / L::VS) & 1, abort_flag, p.status, 6)) { ok = false; break; }
-                tc_fence_after();
-                for (int x = 0; x < 2; ++x) {
-                    const int nx = x ? nB : nA;
-                    const int jx0 = x ? jB0 : jA0;
-                    if (j < jx0 - 1 || j >= nx) continue;
-                    if (j >= jx0) {
-                        if (!issue_pv(x, j - jx0, u)) { ok = false; break; }
-                        if (j + 1 == nx) mma_commit(&o_final[x]);
+            if constexpr (!GENERAL) {
+                // full causal or no mask: both tiles start at K/V tile 0
+                for (int j = 0; ok && j < nmax; ++j) {
+                    if (!mbar_wait(&v_full[j % L::VS], (j / L::VS) & 1, abort_flag, p.status, 6)) {
+                        ok = false;
+                        break;
                     }
-                    if (j + 1 < nx) {
-                        // S_x(j+1) overwrites P_x(j), which the MMAs just issued read first
-                        if (!wait_k(u + 1)) { ok = false; break; }
-                        issue_s(x, u + 1);
+                    tc_fence_after();
+                    for (int x = 0; x < 2; ++x) {
+                        const int nx = x ? nB : nA;
+                        if (j >= nx) continue;
+                        if (!issue_pv(x, j, j)) { ok = false; break; }
+                        if (j + 1 < nx) {
+                            // S_x(j+1) overwrites P_x(j), which the MMAs just issued read first
+                            if (!wait_k(j + 1)) { ok = false; break; }
+                            issue_s(x, j + 1);
+                        } else {
+                            mma_commit(&o_final[x]);
+                        }
                     }
+                    if (!ok) break;
+                    mma_commit(&v_empty[j % L::VS]);
+                    if (j + 1 < nmax) mma_commit(&k_empty[(j + 1) % L::KS]);
                 }
-                if (!ok) break;
-                mma_commit(&v_empty[u % L::VS]);
-                if (j + 1 < nmax) mma_commit(&k_empty[(u + 1) % L::KS]);
+            } else {
+                for (int j = jA0; ok && j < nmax; ++j) {
+                    const int u = j - jA0;
+                    if (!mbar_wait(&v_full[u % L::VS], (u / L::VS) & 1, abort_flag, p.status, 6)) { ok = false; break; }
+                    tc_fence_after();
+                    for (int x = 0; x < 2; ++x) {
+                        const int nx = x ? nB : nA;
+                        const int jx0 = x ? jB0 : jA0;
+                        if (j < jx0 - 1 || j >= nx) continue;
+                        if (j >= jx0) {
+                            if (!issue_pv(x, j - jx0, u)) { ok = false; break; }
+                            if (j + 1 == nx) mma_commit(&o_final[x]);
+                        }
+                        if (j + 1 < nx) {
+                            // S_x(j+1) overwrites P_x(j), which the MMAs just issued read first
+                            if (!wait_k(u + 1)) { ok = false; break; }
+                            issue_s(x, u + 1);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&v_empty[u % L::VS]);
+                    if (j + 1 < nmax) mma_commit(&k_empty[(u + 1) % L::KS]);
+                }
             }
             // every MMA issued above has completed once `drain` flips
             mma_commit(drain);
@@ -319,11 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             const int kv0 = j * kBN;
             const bool need_mask = (kv0 + kBN > N) || (p.causal && kv0 + kBN - 1 > q0) ||
-                                   (p.window > 0 && kv0 < q0 + kBM - p.window);
+                                   (win > 0 && kv0 < q0 + kBM - win);
             if (need_mask) {
                 // visible: lo <= key < hi
                 const int hi = p.causal ? min(N, q0 + row + 1) : N;
-                const int lo = p.window > 0 ? q0 + row - p.window + 1 : 0;
+                const int lo = win > 0 ? q0 + row - win + 1 : 0;
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
                     if (kv0 + c >= hi || kv0 + c < lo) s[c] = __float_as_uint(-INFINITY);
@@ -351,15 +381,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // a row that has seen no visible key yet (its keys start in a later
             // tile of a sliding window) keeps m_ref = -inf: use 0 so that its
             // masked scores give P = 0 rather than -inf - (-inf)
-            const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
+            const float m_use = (GENERAL && m_ref == -INFINITY) ? 0.0f : m_ref;
             const float2 neg_m = make_float2(-m_use, -m_use);
             const float2 sl2x2 = make_float2(sl2, sl2);
             float2 lr01 = make_float2(0.f, 0.f), lr23 = lr01, le01 = lr01, le23 = lr01;
+            // P is written back in chunks of CH scores (CH / 2 packed columns),
+            // which keeps fewer registers live than one 64-column store
+            constexpr int CH = 32;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t pk[32];
+            for (int hh = 0; hh < 128 / CH; ++hh) {
+                uint32_t pk[CH / 2];
 #pragma unroll
-                for (int c = 64 * hh; c < 64 * hh + 64; c += 4) {
+                for (int c = CH * hh; c < CH * hh + CH; c += 4) {
                     const float2 x01 =
                         ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, neg_m);
                     const float2 x23 =
@@ -368,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float p1 = ex2_approx(x01.y);
                     const float p2 = ex2_approx(x23.x);
                     const float p3 = ex2_approx(x23.y);
-                    const int k = (c - 64 * hh) / 2;
+                    const int k = (c - CH * hh) / 2;
                     // l sums the rounded P that the MMA consumes, so O~ / l is an
                     // exactly normalised mix of V rows even when one term dominates
                     if constexpr (BF16) {
@@ -383,9 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     le01 = fadd2(le01, make_float2(p0, p1));
                     le23 = fadd2(le23, make_float2(p2, p3));
                 }
-                // P of keys 64 hh .. + 63 -> columns 32 hh .. + 31 of this row's S,
-                // all of which have been read
-                tmem_st_x32(lane_base + col_s + 32 * hh, pk);
+                // P of keys CH hh .. + CH - 1 -> columns CH / 2 * hh .. of this
+                // row's S, all of which have been read
+                if constexpr (CH == 64)
+                    tmem_st_x32(lane_base + col_s + 32 * hh, pk);
+                else
+                    tmem_st_x16(lane_base + col_s + 16 * hh, pk);
             }
             l_sum += (lr01.x + lr01.y) + (lr23.x + lr23.y);
             l_exact += (le01.x + le01.y) + (le23.x + le23.y);
@@ -432,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float bb = __uint_as_float(o[2 * c + 1]) * inv_l;
                         w[c] = BF16 ? pack_bf16x2(a, bb) : pack_f16x2(a, bb);
                     }
-                    if (p.varlen) {
+                    if (packed) {
                         // packed rows: a 128-row box past this sequence's end
                         // would overwrite the next sequence, so each thread
                         // stores its own row (16-byte stores)
@@ -453,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (!p.varlen) {
+                if (!packed) {
                     fence_proxy_async_smem();
                     named_bar_sync(1 + x, kBM);
                     if (row == 0) {
@@ -464,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (q0 + row < N) {
-                    const size_t li = p.varlen ? (size_t)h * p.total + row0 + q0 + row : (size_t)q_plane * N + q0 + row;
+                    const size_t li = packed ? (size_t)h * p.total + row0 + q0 + row : (size_t)q_plane * N + q0 + row;
                     p.lse[li] = (m_ref + log2f(l_exact)) * 0.69314718055994530942f;
                 }
             }
@@ -488,8 +524,9 @@ cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t st) {
     if (!make_tmap_tiles(&tq, a.q, dt, D, a.lay, a.Hq, kBM) || !make_tmap_tiles(&tk, a.k, dt, D, a.lay, a.Hkv, kBN) ||
         !make_tmap_tiles(&tv, a.v, dt, D, a.lay, a.Hkv, kBN) || !make_tmap_tiles(&to, a.o, dt, D, a.lay, a.Hq, kBM))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::ALLOC);
+    const bool general = a.window > 0 || a.lay.varlen;
+    auto kernel = general ? fwd_kernel<D, BF16, true> : fwd_kernel<D, BF16, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     FwdParams p;
     p.o = a.o;
@@ -506,7 +543,7 @@ cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t st) {
     p.window = a.window;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     const long long grid = (long long)p.nblk * a.B * a.Hq;
-    fwd_kernel<D, BF16><<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, to, p);
+    kernel<<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
