@@ -42,6 +42,7 @@ def _args():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-two-pass", action="store_true", help="skip the deterministic two-pass backward leg")
     ap.add_argument("--no-window", action="store_true", help="skip the sliding-window leg")
+    ap.add_argument("--no-varlen", action="store_true", help="skip the packed variable-length leg")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 leg (outlier workload)")
     return ap.parse_args()
 
@@ -265,6 +266,8 @@ def run_ours(a):
                                                    flush)
     if has_bwd and not a.no_window and w.causal:
         result["window_leg"] = _window_leg(a, w, (q, k, v, o, lse, dO, dq, dk, dv), dev, stream, peaks, flush)
+    if has_bwd and not a.no_varlen and a.workload is None:
+        result["varlen_leg"] = _varlen_leg(a, dev, stream, peaks, flush)
     if not a.no_fp8 and a.workload is None:
         result["fp8_leg"] = _fp8_leg(a, dev, stream, peaks)
     if not a.no_e2e:
@@ -364,6 +367,64 @@ def _window_leg(a, w, t, dev, stream, peaks, flush, window=1024):
             "flops": "visible (query, key) pairs only"}
 
 
+def _varlen_leg(a, dev, stream, peaks, flush, n_seq=8, max_len=8192, Hq=16, d=128):
+    """Packed variable-length batch (fa_fwd_varlen / fa_bwd_varlen, atomic dQ):
+    a seeded mix of 8 causal bf16 sequences of 1 .. 8192 rows, H16 d128,
+    token-major.  FLOPs count each sequence's own causal pairs n (n + 1) / 2."""
+    import torch
+
+    from exact_attention_85_gb300 import _lib
+    from exact_attention_85_gb300.inputs import make_varlen, varlen_lengths
+
+    lengths = varlen_lengths(n_seq, max_len, seed=11)
+    x = make_varlen(lengths, Hq, Hq, d, torch.bfloat16, seed=12)
+    q, k, v, dO = (x[n].to(dev).contiguous() for n in ("q", "k", "v", "dO"))
+    cu = x["cu_seqlens"].to(dev)
+    total = q.shape[0]
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, total), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(_lib.fa_bwd_varlen_workspace_bytes(total, Hq, d, False), dtype=torch.uint8, device=dev)
+    mx = max(lengths)
+    scale = d ** -0.5
+    pairs = sum(n * (n + 1) / 2 for n in lengths)
+    f_fwd = 4.0 * Hq * d * pairs
+    f_bwd = 2.5 * f_fwd
+
+    def fwd():
+        _lib.fa_fwd_varlen(q, k, v, o, lse, cu, mx, True, scale, 0, stream)
+
+    def bwd():
+        _lib.fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu, mx, True, scale, False, ws, 0, stream)
+
+    for _ in range(max(3, a.warmup)):
+        fwd()
+        bwd()
+        flush.zero_()
+    torch.cuda.synchronize()
+    steps = max(3, min(a.steps, 10))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    if _lib.fa_get_device_status(stream) != _lib.FA_OK:
+        raise RuntimeError("a bounded device wait ran out during the packed-batch leg")
+    f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    b_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ftf = f_fwd / (f_ms * 1e-3) / 1e12
+    btf = f_bwd / (b_ms * 1e-3) / 1e12
+    return {"workload": f"packed bf16 H{Hq} d{d} causal, lengths {lengths} (total {total})",
+            "fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4), "fwd_tflops": round(ftf, 1),
+            "bwd_tflops": round(btf, 1), "fwd_frac_of_peak": round(ftf / peaks["bf16_tflops"], 4),
+            "bwd_frac_of_peak": round(btf / peaks["bf16_tflops"], 4), "launches_per_step": 4,
+            "flops": "each sequence's causal pairs only"}
+
+
 def _fp8_leg(a, dev, stream, peaks):
     """The FP8 rows of the path on their own workload (B4 H16 N8192 d128,
     non-causal, 0.1% outliers): random-sign Hadamard + e4m3 quantisation of
@@ -414,11 +475,29 @@ def _fp8_leg(a, dev, stream, peaks):
     q_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     f_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     tflops = w.fwd_flops() / (f_ms * 1e-3) / 1e12
+
+    # the same FP8 operands with the causal mask (half the FLOPs)
+    def fwd_causal():
+        _lib.fa_fwd_fp8(q8, k8, v8, ds[0:1], ds[1:2], ds[2:3], o, lse, True, w.scale, stream)
+
+    for _ in range(3):
+        fwd_causal()
+    torch.cuda.synchronize()
+    evc = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        evc[i][0].record(stream)
+        fwd_causal()
+        evc[i][1].record(stream)
+        flush.zero_()
+    torch.cuda.synchronize()
+    c_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evc)
+    c_tflops = w.fwd_flops() / 2 / (c_ms * 1e-3) / 1e12
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     q_bytes = 3 * q.numel() * (2 + 1)  # algorithmic: read bf16 once, write e4m3 once
     return {"workload": w.name, "fwd_ms": round(f_ms, 4), "fwd_tflops": round(tflops, 1),
             "fwd_frac_of_fp8_peak": round(tflops / fp8_peak, 4),
             "fp8_peak": fp8_peak, "fp8_peak_source": f"2 x {peaks['source']} bf16 burst (nominal FP8/BF16 ratio)",
+            "fwd_causal_ms": round(c_ms, 4), "fwd_causal_tflops": round(c_tflops, 1),
             "quant_ms_3_tensors": round(q_ms, 4),
             "quant_gbs_algorithmic": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
             "quant_frac_of_hbm": round(q_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
