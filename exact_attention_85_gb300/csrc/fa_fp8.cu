@@ -14,8 +14,8 @@
 //                    nearest even, saturating), descale = amax / 448
 // With signs == NULL the rotation is skipped (plain per-tensor FP8).
 //
-// Forward (fwd_fp8_kernel): the structure of the bf16 forward (fa_fwd.cu)
-// with kind::f8f6f4 MMAs: Q, K, V e4m3 in 128-byte-swizzled shared memory
+// Forward (fwd_fp8_kernel): the structure of the bf16 forward (fa_fwd.cu,
+// two Q tiles per CTA) with kind::f8f6f4 MMAs: Q, K, V e4m3 in 128-byte-swizzled shared memory
 // (one 128-byte row = 128 values, so d = 128 is one swizzle atom wide), P
 // quantised to e4m3 in tensor memory as the A operand of O += P V.  Scores are
 // descaled as S = scale * q_descale * k_descale * Q8 K8^T; O is multiplied by
@@ -176,37 +176,46 @@ __global__ void __launch_bounds__(256) hq_quant_kernel(const uint4 *__restrict__
 }
 
 // ----------------------------------------------------------- FP8 forward
+// Two 128-row Q tiles per CTA with ping-ponged softmax warpgroups, as in the
+// bf16 forward: warps 0-3 tile A, 4-7 tile B, warp 8 TMA producer, warp 9
+// MMA issuer.  Tensor memory: S_A [0,128), S_B [128,256), O_A [256,384),
+// O_B [384,512); P (e4m3, 32 columns) overlays the first columns of its own
+// S.  MMA order per K/V tile j: O_A += P_A V_j, S_A(j+1), O_B += P_B V_j,
+// S_B(j+1), so S_X(j+1) completes after O_X += P_X(j) V_j.
 
 constexpr int kBM = 128, kBN = 128, kD = 128;
-constexpr int kThreads = 224;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr float kRescaleThreshold = 4.0f;  // log2 units
 constexpr float kLift = 4.0f;              // P is quantised as 2^(s - m + kLift)
 
 struct Fp8Layout {
     static constexpr int KS = 3, VS = 3;
     static constexpr int TILE = kBM * kD;  // bytes (1 byte per value)
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + TILE;
+    static constexpr int OFF_Q = 0;        // Q_A, Q_B
+    static constexpr int OFF_K = OFF_Q + 2 * TILE;
     static constexpr int OFF_V = OFF_K + KS * TILE;
-    static constexpr int OFF_O = OFF_V + VS * TILE;  // bf16 output staging, 2 boxes of 128 x 64
-    static constexpr int OFF_BAR = OFF_O + kBM * kD * 2;
-    static constexpr int NBAR = 2 + 2 * KS + 2 * VS + 2 + 2 + 1 + 1;  // + q_tmem
+    static constexpr int OFF_O = OFF_V + VS * TILE;  // bf16 output staging: per tile 2 boxes of 128 x 64
+    static constexpr int OTILE = kBM * kD * 2;
+    static constexpr int OFF_BAR = OFF_O + 2 * OTILE;
+    // q_full, k_full[KS], k_empty[KS], v_full[VS], v_empty[VS], s_full[2],
+    // p_full[2], o_final[2], drain
+    static constexpr int NBAR = 1 + 2 * KS + 2 * VS + 2 + 2 + 2 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int ALLOC = BYTES + 1024;
+    static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
 struct Fp8Params {
     float *lse;
     const float *q_descale, *k_descale, *v_descale;
     unsigned int *status;
-    int Hq, Hkv, N, nqt, causal;
+    int Hq, Hkv, N, nblk, causal;  // nblk: 256-row blocks per head
     float scale_log2;
 };
 
-// S buffers [0,128), [128,256); O [256,384); Q [384,416) (4 e4m3 per column).
-// P (e4m3, 32 columns) overlays the first columns of its own S buffer.
-constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;
+constexpr uint32_t kColS = 0, kColO = 256;  // + 128 per tile
 
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -217,44 +226,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
     uint64_t *q_full = bars;
-    uint64_t *q_tmem = bars + 1;
-    uint64_t *k_full = q_tmem + 1;
+    uint64_t *k_full = q_full + 1;
     uint64_t *k_empty = k_full + L::KS;
     uint64_t *v_full = k_empty + L::KS;
     uint64_t *v_empty = v_full + L::VS;
-    uint64_t *s_full = v_empty + L::VS;
-    uint64_t *p_full = s_full + 2;
-    uint64_t *o_done = p_full + 2;
-    uint64_t *drain = o_done + 1;
+    uint64_t *s_full = v_empty + L::VS;  // [2], one per tile
+    uint64_t *p_full = s_full + 2;       // [2]
+    uint64_t *o_final = p_full + 2;      // [2]
+    uint64_t *drain = o_final + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / p.nqt;
-    const int qt_lin = blockIdx.x - bh * p.nqt;
-    const int qt = p.causal ? (p.nqt - 1 - qt_lin) : qt_lin;
+    // consecutive CTAs share a head (K/V stay in L2); causal blocks longest first
+    const int bh = blockIdx.x / p.nblk;
+    const int t_lin = blockIdx.x - bh * p.nblk;
+    const int t = p.causal ? (p.nblk - 1 - t_lin) : t_lin;
     const int b = bh / p.Hq;
     const int h = bh - b * p.Hq;
     const int hk = h / (p.Hq / p.Hkv);
-    const int q0 = qt * kBM;
+    const int q0a = t * 2 * kBM;
     const int nkv_all = (p.N + kBN - 1) / kBN;
-    const int nkv = p.causal ? min(qt + 1, nkv_all) : nkv_all;
+    // K/V tiles each Q tile visits; 0 for a tile that lies entirely past N
+    const int nA = p.causal ? min(q0a / kBN + 1, nkv_all) : nkv_all;
+    const int nB = q0a + kBM >= p.N ? 0 : (p.causal ? min((q0a + kBM) / kBN + 1, nkv_all) : nkv_all);
+    const int nmax = max(nA, nB);
     const int kv_plane = b * p.Hkv + hk;
     const int q_plane = b * p.Hq + h;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(q_tmem, kBM);
         for (int s = 0; s < L::KS; ++s) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
         for (int s = 0; s < L::VS; ++s) { mbar_init(&v_full[s], 1); mbar_init(&v_empty[s], 1); }
-        for (int s = 0; s < 2; ++s) { mbar_init(&s_full[s], 1); mbar_init(&p_full[s], kBM); }
-        mbar_init(o_done, 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&s_full[x], 1);
+            mbar_init(&p_full[x], kBM);
+            mbar_init(&o_final[x], 1);
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
@@ -263,133 +277,140 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
-        // ---------------------------------------------------- Q + K producer
+    if (warp == kProducerWarp) {
+        // -------------------------------------------------------- TMA producer
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
-            mbar_arrive_expect_tx(q_full, L::TILE);
-            tma_load_3d(smem + L::OFF_Q, &tm_q, q_full, 0, q0, q_plane);
-            int j = 0;
-            for (; j < nkv; ++j) {
-                const int s = j % L::KS;
-                if (j >= L::KS && !mbar_wait(&k_empty[s], ((j / L::KS) + 1) & 1, abort_flag, p.status, 41)) break;
-                mbar_arrive_expect_tx(&k_full[s], L::TILE);
-                tma_load_3d(smem + L::OFF_K + s * L::TILE, &tm_k, &k_full[s], 0, j * kBN, kv_plane);
-            }
-            if (*abort_flag) {
-                for (int t = max(0, j - L::KS); t < j; ++t)
-                    mbar_wait_drain(&k_full[t % L::KS], (t / L::KS) & 1, 10000000ull);
-                mbar_wait_drain(q_full, 0, 10000000ull);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 6) {
-        // -------------------------------------------------------- V producer
-        if (lane == 0) {
             prefetch_tmap(&tm_v);
-            int j = 0;
-            for (; j < nkv; ++j) {
-                const int s = j % L::VS;
-                if (j >= L::VS && !mbar_wait(&v_empty[s], ((j / L::VS) + 1) & 1, abort_flag, p.status, 42)) break;
-                mbar_arrive_expect_tx(&v_full[s], L::TILE);
-                tma_load_3d(smem + L::OFF_V + s * L::TILE, &tm_v, &v_full[s], 0, j * kBN, kv_plane);
+            const int ntq = nB > 0 ? 2 : 1;
+            mbar_arrive_expect_tx(q_full, ntq * L::TILE);
+            for (int x = 0; x < ntq; ++x)
+                tma_load_3d(smem + L::OFF_Q + x * L::TILE, &tm_q, q_full, 0, q0a + x * kBM, q_plane);
+            int nk = 0, nv = 0;
+            for (int j = 0; j < nmax; ++j) {
+                const int ks = j % L::KS;
+                if (j >= L::KS && !mbar_wait(&k_empty[ks], ((j / L::KS) + 1) & 1, abort_flag, p.status, 41)) break;
+                mbar_arrive_expect_tx(&k_full[ks], L::TILE);
+                tma_load_3d(smem + L::OFF_K + ks * L::TILE, &tm_k, &k_full[ks], 0, j * kBN, kv_plane);
+                ++nk;
+                const int vs = j % L::VS;
+                if (j >= L::VS && !mbar_wait(&v_empty[vs], ((j / L::VS) + 1) & 1, abort_flag, p.status, 42)) break;
+                mbar_arrive_expect_tx(&v_full[vs], L::TILE);
+                tma_load_3d(smem + L::OFF_V + vs * L::TILE, &tm_v, &v_full[vs], 0, j * kBN, kv_plane);
+                ++nv;
             }
             if (*abort_flag) {
-                for (int t = max(0, j - L::VS); t < j; ++t)
-                    mbar_wait_drain(&v_full[t % L::VS], (t / L::VS) & 1, 10000000ull);
+                // let copies already in flight land before the CTA exits
+                mbar_wait_drain(q_full, 0, 10000000ull);
+                for (int u = max(0, nk - L::KS); u < nk; ++u)
+                    mbar_wait_drain(&k_full[u % L::KS], (u / L::KS) & 1, 10000000ull);
+                for (int u = max(0, nv - L::VS); u < nv; ++u)
+                    mbar_wait_drain(&v_full[u % L::VS], (u / L::VS) & 1, 10000000ull);
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             // kind::f8f6f4, e4m3 (format 0) for both operands, fp32 accumulate
             constexpr uint32_t idesc_s = make_idesc(kBM, kBN, 0u, false, false);
             constexpr uint32_t idesc_pv = make_idesc(kBM, kD, 0u, false, true);
+            const uint64_t q_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_Q), 16, 1024);
             const uint64_t k_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);
             const uint64_t v_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_V), 0, 1024);
-            // Q is in tensor memory once the softmax warps have copied it
-            bool ok = mbar_wait(q_tmem, 0, abort_flag, p.status, 43);
-            tc_fence_after();
+            int k_ready = -1;  // highest K tile whose arrival has been observed
 
-            auto issue_pv = [&](int t) -> bool {
-                const int pb = t & 1;
-                if (!mbar_wait(&p_full[pb], (t >> 1) & 1, abort_flag, p.status, 44)) return false;
-                const int vs = t % L::VS;
-                if (!mbar_wait(&v_full[vs], (t / L::VS) & 1, abort_flag, p.status, 45)) return false;
+            auto wait_k = [&](int j) -> bool {
+                if (j <= k_ready) return true;
+                if (!mbar_wait(&k_full[j % L::KS], (j / L::KS) & 1, abort_flag, p.status, 43)) return false;
                 tc_fence_after();
-                const uint64_t v_desc = sdesc_advance(v_desc0, vs * L::TILE);
-                const uint32_t p_col = tmem + kColS + pb * kBN;  // P overlays its S buffer
-                // B = V: head dim contiguous (MN-major), 32 keys = 32 rows of 128 B
-                mma_f8_ts(tmem + kColO, p_col, v_desc, idesc_pv, t > 0 ? 1u : 0u);
+                k_ready = j;
+                return true;
+            };
+            // S_x(j) = Q_x K_j^T: both operands K-major e4m3, 32 values = 32
+            // bytes per step inside the 128-byte row
+            auto issue_s = [&](int x, int j) {
+                const uint64_t q_desc = sdesc_advance(q_desc0, x * L::TILE);
+                const uint64_t k_desc = sdesc_advance(k_desc0, (j % L::KS) * L::TILE);
 #pragma unroll
-                for (int kk = 1; kk < kBN / 32; ++kk)
-                    mma_f8_ts(tmem + kColO, p_col + kk * 8, sdesc_advance(v_desc, kk * 32 * 128), idesc_pv, 1u);
-                mma_commit(o_done);
-                mma_commit(&v_empty[vs]);
+                for (int kk = 0; kk < kD / 32; ++kk)
+                    mma_f8_ss(tmem + kColS + x * 128, sdesc_advance(q_desc, kk * 32), sdesc_advance(k_desc, kk * 32),
+                              idesc_s, kk > 0 ? 1u : 0u);
+                mma_commit(&s_full[x]);
+            };
+            // O_x += P_x(j) V_j: A = P from tensor memory (32 keys = 8 columns
+            // per step), B = V with the head dim contiguous (MN-major), 32
+            // keys = 32 rows of 128 bytes per step
+            auto issue_pv = [&](int x, int j) -> bool {
+                if (!mbar_wait(&p_full[x], j & 1, abort_flag, p.status, 44)) return false;
+                tc_fence_after();
+                const uint64_t v_desc = sdesc_advance(v_desc0, (j % L::VS) * L::TILE);
+                const uint32_t p_col = tmem + kColS + x * 128;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 32; ++kk)
+                    mma_f8_ts(tmem + kColO + x * 128, p_col + kk * 8, sdesc_advance(v_desc, kk * 32 * 128), idesc_pv,
+                              (j > 0 || kk > 0) ? 1u : 0u);
                 return true;
             };
 
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int ks = j % L::KS;
-                if (!mbar_wait(&k_full[ks], (j / L::KS) & 1, abort_flag, p.status, 46)) { ok = false; break; }
+            bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 45);
+            if (ok) {
                 tc_fence_after();
-                const uint64_t k_desc = sdesc_advance(k_desc0, ks * L::TILE);
-                const uint32_t s_col = tmem + kColS + (j & 1) * kBN;
-                // A = Q from tensor memory (32 values = 8 columns per step), B = K
-#pragma unroll
-                for (int kk = 0; kk < kD / 32; ++kk)
-                    mma_f8_ts(s_col, tmem + kColQ + kk * 8, sdesc_advance(k_desc, kk * 32), idesc_s, kk > 0 ? 1u : 0u);
-                mma_commit(&s_full[j & 1]);
-                mma_commit(&k_empty[ks]);
-                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+                ok = wait_k(0);
             }
-            if (ok && nkv > 0) issue_pv(nkv - 1);
+            if (ok) {
+                issue_s(0, 0);
+                if (nB > 0) issue_s(1, 0);
+                mma_commit(&k_empty[0]);
+            }
+            for (int j = 0; ok && j < nmax; ++j) {
+                if (!mbar_wait(&v_full[j % L::VS], (j / L::VS) & 1, abort_flag, p.status, 46)) { ok = false; break; }
+                tc_fence_after();
+                for (int x = 0; x < 2; ++x) {
+                    const int nx = x ? nB : nA;
+                    if (j >= nx) continue;
+                    if (!issue_pv(x, j)) { ok = false; break; }
+                    if (j + 1 < nx) {
+                        // S_x(j+1) overwrites P_x(j), which the MMAs just issued read first
+                        if (!wait_k(j + 1)) { ok = false; break; }
+                        issue_s(x, j + 1);
+                    } else {
+                        mma_commit(&o_final[x]);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&v_empty[j % L::VS]);
+                if (j + 1 < nmax) mma_commit(&k_empty[(j + 1) % L::KS]);
+            }
+            // every MMA issued above has completed once `drain` flips
             mma_commit(drain);
             mbar_wait_drain(drain, 0, 100000000ull);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ softmax + epilogue
-        const int row = threadIdx.x;  // 0..127 == TMEM lane
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const int x = warp >> 2;  // tile
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;  // query row within the tile == TMEM lane
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t col_s = kColS + x * 128, col_o = kColO + x * 128;
+        const int q0 = q0a + x * kBM;
+        const int nx = x ? nB : nA;
         const float sl2 = p.scale_log2 * (*p.q_descale) * (*p.k_descale);
         float m_ref = -INFINITY;
         float l_sum = 0.0f;    // sum of the quantised P (lifted): normalises O
         float l_exact = 0.0f;  // sum of the unquantised P (lifted): gives L
         bool ok = true;
-        uint32_t s[128];
 
-        {
-            // copy this row of Q (128 e4m3 bytes) from the swizzled shared tile
-            // into tensor memory
-            const bool got_q = mbar_wait(q_full, 0, abort_flag, p.status, 50);
-            ok = __all_sync(0xffffffffu, got_q);
-            if (ok) {
-                uint32_t qv[32];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint4 u =
-                        *reinterpret_cast<const uint4 *>(smem + L::OFF_Q + row * 128 + ((k ^ (row & 7)) << 4));
-                    qv[k * 4 + 0] = u.x;
-                    qv[k * 4 + 1] = u.y;
-                    qv[k * 4 + 2] = u.z;
-                    qv[k * 4 + 3] = u.w;
-                }
-                tmem_st_x32(lane_base + kColQ, qv);
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(q_tmem);
-            }
-        }
-
-        for (int j = 0; ok && j < nkv; ++j) {
-            const int sb = j & 1;
-            const bool got_s = mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag, p.status, 47);
+        for (int j = 0; ok && j < nx; ++j) {
+            // every lane waits, then the warp votes: the tcgen05.ld/st below
+            // are warp-collective (.sync.aligned) and need all 32 lanes
+            const bool got_s = mbar_wait(&s_full[x], j & 1, abort_flag, p.status, 47);
             if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t s_addr = lane_base + kColS + sb * kBN;
+            uint32_t s[128];
+            const uint32_t s_addr = lane_base + col_s;
             tmem_ld_x32(s_addr + 0, s + 0);
             tmem_ld_x32(s_addr + 32, s + 32);
             tmem_ld_x32(s_addr + 64, s + 64);
@@ -426,107 +447,112 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = mx;
                 rescale = true;
             }
+            __syncwarp();  // reconverge after the per-row branches above
             const float2 bias = make_float2(kLift - m_ref, kLift - m_ref);
             const float2 sl2x2 = make_float2(sl2, sl2);
             float2 le01 = make_float2(0.f, 0.f), le23 = le01;
             // the sum of the quantised P is accumulated in fp16 pairs over 32
             // scores (at most 32 x 256: exact range, 11-bit precision) and then
             // widened, which costs one conversion and one add per two scores
-            uint32_t hacc0 = 0u, hacc1 = 0u;
             float lr = 0.0f;
-            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                const float2 x01 = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, bias);
-                const float2 x23 = ffma2(make_float2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2, bias);
-                const float p0 = ex2_approx(x01.x);
-                const float p1 = ex2_approx(x01.y);
-                const float p2 = ex2_approx(x23.x);
-                const float p3 = ex2_approx(x23.y);
-                const uint32_t w01 = cvt_e4m3x2(p0, p1);
-                const uint32_t w23 = cvt_e4m3x2(p2, p3);
-                pk[c / 4] = w01 | (w23 << 16);
-                hacc0 = hadd2_u32(hacc0, e4m3x2_to_h2(w01));
-                hacc1 = hadd2_u32(hacc1, e4m3x2_to_h2(w23));
-                if ((c & 31) == 28) {  // every 32 scores: widen and restart
-                    const float2 f0 = unpack2<false>(hacc0);
-                    const float2 f1 = unpack2<false>(hacc1);
-                    lr += (f0.x + f0.y) + (f1.x + f1.y);
-                    hacc0 = 0u;
-                    hacc1 = 0u;
+            for (int hh = 0; hh < 4; ++hh) {
+                uint32_t pk[8];
+                uint32_t hacc0 = 0u, hacc1 = 0u;
+#pragma unroll
+                for (int c = 32 * hh; c < 32 * hh + 32; c += 4) {
+                    const float2 x01 =
+                        ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, bias);
+                    const float2 x23 =
+                        ffma2(make_float2(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), sl2x2, bias);
+                    const float p0 = ex2_approx(x01.x);
+                    const float p1 = ex2_approx(x01.y);
+                    const float p2 = ex2_approx(x23.x);
+                    const float p3 = ex2_approx(x23.y);
+                    const uint32_t w01 = cvt_e4m3x2(p0, p1);
+                    const uint32_t w23 = cvt_e4m3x2(p2, p3);
+                    pk[(c - 32 * hh) / 4] = w01 | (w23 << 16);
+                    hacc0 = hadd2_u32(hacc0, e4m3x2_to_h2(w01));
+                    hacc1 = hadd2_u32(hacc1, e4m3x2_to_h2(w23));
+                    le01 = fadd2(le01, make_float2(p0, p1));
+                    le23 = fadd2(le23, make_float2(p2, p3));
                 }
-                le01 = fadd2(le01, make_float2(p0, p1));
-                le23 = fadd2(le23, make_float2(p2, p3));
+                const float2 f0 = unpack2<false>(hacc0);
+                const float2 f1 = unpack2<false>(hacc1);
+                lr += (f0.x + f0.y) + (f1.x + f1.y);
+                // P of keys 32 hh .. + 31 -> columns 8 hh .. + 7 of this row's S,
+                // all of which have been read
+                tmem_st_x8(lane_base + col_s + 8 * hh, pk);
             }
             l_sum += lr;
             l_exact += (le01.x + le01.y) + (le23.x + le23.y);
-            __syncwarp();
-            tmem_st_x32(lane_base + kColS + sb * kBN, pk);  // P overlays the S row just read
-
-            if (j >= 1) {
-                const bool got_o = mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status, 48);
-                if (!__all_sync(0xffffffffu, got_o)) { ok = false; break; }
-                if (__any_sync(0xffffffffu, rescale)) {
-                    tc_fence_after();
+            // O_x already holds P_x(0..j-1) V (S_x(j) was issued after the last
+            // P.V of this tile), and P_x(j) V is issued only after p_full;
+            // warp-uniform branch, lanes that keep their max use alpha = 1
+            if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < kD; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld_x32(lane_base + kColO + c0, o);
-                        tmem_ld_wait_x32(o);
+                for (int c0 = 0; c0 < kD; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld_x32(lane_base + col_o + c0, o);
+                    tmem_ld_wait_x32(o);
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                        tmem_st_x32(lane_base + kColO + c0, o);
-                    }
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                    tmem_st_x32(lane_base + col_o + c0, o);
                 }
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_full[sb]);
+            mbar_arrive(&p_full[x]);
         }
 
-        if (ok && nkv > 0) ok = mbar_wait(o_done, (nkv - 1) & 1, abort_flag, p.status, 49);
-        __syncwarp();
-        ok = named_bar_and(1, kBM, ok);
-        if (ok) {
-            tc_fence_after();
-            // O = v_descale * O~ / l, bf16, staged in the 128-byte-swizzled
-            // layout of two 64-column output boxes
-            const float f = (*p.v_descale) / l_sum;
-            uint8_t *stage = smem + L::OFF_O;
+        if (nx > 0) {  // uniform across the warpgroup
+            if (ok) ok = mbar_wait(&o_final[x], 0, abort_flag, p.status, 49);
+            __syncwarp();
+            // uniform decision across the tile's 128 threads (the epilogue has a
+            // named barrier that all of them must reach)
+            ok = named_bar_and(1 + x, kBM, ok);
+            if (ok) {
+                tc_fence_after();
+                // O = v_descale * O~ / l, bf16, staged in the 128-byte-swizzled
+                // layout of two 64-column output boxes
+                const float f = (*p.v_descale) / l_sum;
+                uint8_t *stage = smem + L::OFF_O + x * L::OTILE;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kD; c0 += 32) {
-                uint32_t o[32];
-                tmem_ld_x32(lane_base + kColO + c0, o);
-                tmem_ld_wait_x32(o);
-                uint32_t w[16];
+                for (int c0 = 0; c0 < kD; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld_x32(lane_base + col_o + c0, o);
+                    tmem_ld_wait_x32(o);
+                    uint32_t w[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * f, __uint_as_float(o[2 * c + 1]) * f);
-                uint8_t *rowp = stage + (c0 >> 6) * (kBM * 128) + row * 128;
+                    for (int c = 0; c < 16; ++c)
+                        w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * f, __uint_as_float(o[2 * c + 1]) * f);
+                    uint8_t *rowp = stage + (c0 >> 6) * (kBM * 128) + row * 128;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = ((c0 & 63) >> 3) + q;
-                    *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (row & 7)) << 4)) =
-                        make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    for (int q = 0; q < 4; ++q) {
+                        const int chunk = ((c0 & 63) >> 3) + q;
+                        *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (row & 7)) << 4)) =
+                            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                    }
                 }
+                fence_proxy_async_smem();
+                named_bar_sync(1 + x, kBM);
+                if (row == 0) {
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_store_3d(&tm_o, stage + bx * (kBM * 128), bx * 64, q0, q_plane);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
+                if (q0 + row < p.N)
+                    p.lse[(size_t)q_plane * p.N + q0 + row] =
+                        (m_ref + log2f(l_exact) - kLift) * 0.69314718055994530942f;
             }
-            fence_proxy_async_smem();
-            named_bar_sync(1, kBM);
-            if (row == 0) {
-                for (int bx = 0; bx < 2; ++bx) tma_store_3d(&tm_o, stage + bx * (kBM * 128), bx * 64, q0, q_plane);
-                bulk_commit();
-                bulk_wait_read_all();
-            }
-            if (q0 + row < p.N)
-                p.lse[(size_t)q_plane * p.N + q0 + row] =
-                    (m_ref + log2f(l_exact) - kLift) * 0.69314718055994530942f;
         }
         __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -581,10 +607,10 @@ cudaError_t launch_fwd_fp8(const Fp8FwdArgs &a, cudaStream_t st) {
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.N = a.N;
-    p.nqt = (a.N + kBM - 1) / kBM;
+    p.nblk = (a.N + 2 * kBM - 1) / (2 * kBM);
     p.causal = a.causal;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const long long grid = (long long)p.nqt * a.B * a.Hq;
+    const long long grid = (long long)p.nblk * a.B * a.Hq;
     fwd_fp8_kernel<<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
