@@ -357,13 +357,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool wmask = win > 0 && (q_base + hf * 64 + 63 - kv0 >= win);
             uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
 #pragma unroll
+            // S^T and dP^T of chunk ch + 1 load while chunk ch is computed
+            // (two register buffers; a wait covers every load issued so far)
+            uint32_t sbuf[2][16], dbuf[2][16];
+            tmem_ld_x16(lane_base + kColS + hf * 64, sbuf[0]);
+            tmem_ld_x16(lane_base + kColDP + hf * 64, dbuf[0]);
+            tmem_ld_wait_x16(sbuf[0]);
+            tmem_ld_wait_x16(dbuf[0]);
+#pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 const int qc = hf * 64 + ch * 16;  // first query column of this chunk
-                uint32_t s[16], dp[16];
-                tmem_ld_x16(lane_base + kColS + qc, s);
-                tmem_ld_x16(lane_base + kColDP + qc, dp);
-                tmem_ld_wait_x16(s);
-                tmem_ld_wait_x16(dp);
+                uint32_t *s = sbuf[ch & 1];
+                uint32_t *dp = dbuf[ch & 1];
+                if (ch < 3) {
+                    tmem_ld_x16(lane_base + kColS + qc + 16, sbuf[(ch + 1) & 1]);
+                    tmem_ld_x16(lane_base + kColDP + qc + 16, dbuf[(ch + 1) & 1]);
+                }
                 const float *nl2 = ld_smem + st * 2 * kBQ + qc;          // -L log2(e)
                 const float *dsm = ld_smem + st * 2 * kBQ + kBQ + qc;    // D
                 const int q_first = q_base + qc;
@@ -413,6 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q = 0; q < 2; ++q)
                         *reinterpret_cast<uint4 *>(ds_row + (((2 * ch + q) ^ (c & 7)) << 4)) =
                             make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+                }
+                if (ch < 3) {
+                    tmem_ld_wait_x16(sbuf[(ch + 1) & 1]);
+                    tmem_ld_wait_x16(dbuf[(ch + 1) & 1]);
                 }
             }
             if constexpr (DQ) fence_proxy_async_smem();
