@@ -66,9 +66,9 @@ struct BwdLayout {
     static constexpr int OFF_DS = OFF_QD + QS * 2 * TILE_Q;
     static constexpr int OFF_LD = OFF_DS + DS_BYTES;  // stage s: L2[128], D[128]
     static constexpr int OFF_BAR = OFF_LD + QS * 2 * kBQ * 4;
-    // kv_full, qd_full[QS], qd_empty[QS], sdp_full[2], ds_ready[2], dq_full[2],
-    // dq_free[2], acc_done, drain
-    static constexpr int NBAR = 1 + 2 * QS + 8 + 2;
+    // kv_full, qd_full[QS], qd_empty[QS], sdp_full, ds_ready, dq_full, dq_free,
+    // acc_done, drain
+    static constexpr int NBAR = 1 + 2 * QS + 4 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SLACK = 512;  // room to align the dynamic shared base up to 1024
@@ -90,11 +90,7 @@ struct BwdParams {
     float scale, scale_log2;
 };
 
-// tensor-memory columns: per 64-query half-tile buffer b (b = 0, 1)
-//   S^T  [64 b, 64 b + 64)        -> P^T / dS^T over it (16-bit pairs)
-//   dP^T [128 + 64 b, .. + 64)    -> dQ^T over it (lane = head-dim index)
-//   dV [256, 256 + d), dK [384, 384 + d)
-constexpr int kHQ = 64;  // queries per half-tile
+// tensor-memory columns
 constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 128, kColDV = 256, kColDK = 384;
 
 // DQ = false builds the first pass of the deterministic two-pass backward:
@@ -119,11 +115,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *kv_full = bars;
     uint64_t *qd_full = bars + 1;
     uint64_t *qd_empty = qd_full + QS;
-    uint64_t *sdp_full = qd_empty + QS;  // [2] per half-tile buffer
-    uint64_t *ds_ready = sdp_full + 2;   // [2]
-    uint64_t *dq_full = ds_ready + 2;    // [2]
-    uint64_t *dq_free = dq_full + 2;     // [2]
-    uint64_t *acc_done = dq_free + 2;
+    uint64_t *sdp_full = qd_empty + QS;
+    uint64_t *ds_ready = sdp_full + 1;
+    uint64_t *dq_full = ds_ready + 1;
+    uint64_t *dq_free = dq_full + 1;
+    uint64_t *acc_done = dq_free + 1;
     uint64_t *drain = acc_done + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
@@ -159,7 +155,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i_end = win > 0 ? min(nq, (kv0 + kBKV + win - 2) / kBQ + 1) : nq;
     const int n_i = i_end - i_start;
     const int n_it = G * n_i;
-    const int n_u = 2 * n_it;  // 64-query half-tiles: u = 2 it + h uses buffer h
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
@@ -169,12 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&qd_full[s], 33);
             mbar_init(&qd_empty[s], 1);
         }
-        for (int x = 0; x < 2; ++x) {
-            mbar_init(&sdp_full[x], 1);
-            mbar_init(&ds_ready[x], kSoftmaxThreads);
-            mbar_init(&dq_full[x], 1);
-            mbar_init(&dq_free[x], kReadoutThreads / 2);  // one group of 4 read-out warps per buffer
-        }
+        mbar_init(sdp_full, 1);
+        mbar_init(ds_ready, kSoftmaxThreads);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_free, kReadoutThreads);
         mbar_init(acc_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -247,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t fmt = BF16 ? 1u : 0u;
-            constexpr uint32_t idesc_sdp = make_idesc(kBKV, kHQ, fmt, false, false);  // K-major both
+            constexpr uint32_t idesc_sdp = make_idesc(kBKV, kBQ, fmt, false, false);  // K-major both
             constexpr uint32_t idesc_acc = make_idesc(kBKV, D, fmt, false, true);     // A tmem, B MN-major
-            constexpr uint32_t idesc_dq = make_idesc(kBKV, kHQ, fmt, true, true);     // A, B MN-major
+            constexpr uint32_t idesc_dq = make_idesc(kBKV, kBQ, fmt, true, true);     // A, B MN-major
             // one descriptor per operand tile; steps are derived by sdesc_advance
             const uint64_t k_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_K), 16, 1024);  // K-major
             const uint64_t v_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_V), 16, 1024);
@@ -260,90 +253,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dok_desc0 = make_sdesc_sw128(smem_u32(do_stage(0)), 16, 1024);
             const uint64_t qm_desc0 = make_sdesc_sw128(smem_u32(q_stage(0)), L::BOX_Q, 1024);    // MN-major
             const uint64_t dom_desc0 = make_sdesc_sw128(smem_u32(do_stage(0)), L::BOX_Q, 1024);
-            // dS^T of half-tile buffer h: one 64-query box (MN-major B, 128 bytes per key row)
-            const uint64_t ds_desc0 = make_sdesc_sw128(smem_u32(smem + L::OFF_DS), L::DS_BOX, 1024);
+            // dS^T rows of 128 queries = two 64-query boxes (MN-major B, LBO = box stride)
+            const uint64_t ds_desc = make_sdesc_sw128(smem_u32(smem + L::OFF_DS), L::DS_BOX, 1024);
             constexpr uint32_t kStage = 2 * L::TILE_Q;  // bytes between Q/dO stages
-            constexpr uint32_t kHalf = kHQ * 128;       // bytes of 64 rows inside a 64-column box
             bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 22);
 
-            // S^T = K_j Q_u^T -> S^T buffer h, dP^T = V_j dO_u^T -> dP^T buffer h
-            // for the 64 queries of half-tile u (N = 64: rows 64 h .. of the Q tile)
-            auto issue_sdp = [&](int u) -> bool {
-                const int h = u & 1;
-                const int it = u >> 1;
-                const int st = it % QS;
-                if (h == 0) {  // first half of a Q tile: wait for its copies
-                    if (!mbar_wait(&qd_full[st], (it / QS) & 1, abort_flag, p.status, 23)) return false;
-                    tc_fence_after();
-                }
-                const uint64_t q_desc = sdesc_advance(qk_desc0, st * kStage + h * kHalf);
-                const uint64_t do_desc = sdesc_advance(dok_desc0, st * kStage + h * kHalf);
+            // S^T = K_j Q_t^T -> [0, 128) and dP^T = V_j dO_t^T -> [128, 256)
+            auto issue_sdp = [&](int t) -> bool {
+                const int st = t % QS;
+                if (!mbar_wait(&qd_full[st], (t / QS) & 1, abort_flag, p.status, 23)) return false;
+                tc_fence_after();
+                const uint64_t q_desc = sdesc_advance(qk_desc0, st * kStage);
+                const uint64_t do_desc = sdesc_advance(dok_desc0, st * kStage);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
                     const uint32_t oq = (kk >> 2) * L::BOX_Q + (kk & 3) * 32;
-                    mma_f16_ss(tmem + kColS + h * kHQ, sdesc_advance(k_desc, okv), sdesc_advance(q_desc, oq),
-                               idesc_sdp, kk > 0 ? 1u : 0u);
+                    mma_f16_ss(tmem + kColS, sdesc_advance(k_desc, okv), sdesc_advance(q_desc, oq), idesc_sdp,
+                               kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
                     const uint32_t oq = (kk >> 2) * L::BOX_Q + (kk & 3) * 32;
-                    mma_f16_ss(tmem + kColDP + h * kHQ, sdesc_advance(v_desc, okv), sdesc_advance(do_desc, oq),
-                               idesc_sdp, kk > 0 ? 1u : 0u);
+                    mma_f16_ss(tmem + kColDP, sdesc_advance(v_desc, okv), sdesc_advance(do_desc, oq), idesc_sdp,
+                               kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&sdp_full[h]);
+                mma_commit(sdp_full);
                 return true;
             };
 
             if (ok) ok = issue_sdp(0);
-            for (int u = 0; ok && u < n_u; ++u) {
-                const int h = u & 1;
-                const int it = u >> 1;
+            for (int it = 0; ok && it < n_it; ++it) {
                 const int st = it % QS;
-                if (u + 1 < n_u) {
-                    // S^T / dP^T of the next half-tile run on the tensor cores while
-                    // the softmax warps work on this one.  Its buffer last held
-                    // P^T / dS^T of half-tile u - 1 (read by MMAs issued before) and
-                    // dQ^T of u - 1 (read out once dq_free flips).
-                    if constexpr (DQ) {
-                        if (u >= 1 && !mbar_wait(&dq_free[h ^ 1], ((u - 1) >> 1) & 1, abort_flag, p.status, 25)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                    }
-                    if (!issue_sdp(u + 1)) { ok = false; break; }
-                }
-                if (!mbar_wait(&ds_ready[h], (u >> 1) & 1, abort_flag, p.status, 24)) { ok = false; break; }
+                if (!mbar_wait(ds_ready, it & 1, abort_flag, p.status, 24)) { ok = false; break; }
                 tc_fence_after();
-                // dQ_u^T = K_j^T dS_u^T -> dP^T buffer h (lane = head-dim index);
+                // dQ_i^T = K_j^T dS_i^T -> [128, 256) (lane = head-dim index);
                 // 16 keys = 16 rows = 2048 bytes of both operands per step
                 if constexpr (DQ) {
-                    const uint64_t ds_desc = sdesc_advance(ds_desc0, h * L::DS_BOX);
 #pragma unroll
                     for (int kk = 0; kk < kBKV / 16; ++kk)
-                        mma_f16_ss(tmem + kColDQ + h * kHQ, sdesc_advance(kt_desc, kk * 2048),
+                        mma_f16_ss(tmem + kColDQ, sdesc_advance(kt_desc, kk * 2048),
                                    sdesc_advance(ds_desc, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
-                    mma_commit(&dq_full[h]);
+                    mma_commit(dq_full);
                 }
-                const uint64_t qm_desc = sdesc_advance(qm_desc0, st * kStage + h * kHalf);
-                const uint64_t dom_desc = sdesc_advance(dom_desc0, st * kStage + h * kHalf);
-                const uint32_t acc_first = u > 0 ? 1u : 0u;
-                // dV_j += P^T dO_u and dK_j += dS^T Q_u (A from tensor memory;
+                const uint64_t qm_desc = sdesc_advance(qm_desc0, st * kStage);
+                const uint64_t dom_desc = sdesc_advance(dom_desc0, st * kStage);
+                const uint32_t acc_first = it > 0 ? 1u : 0u;
+                // dV_j += P^T dO_i and dK_j += dS^T Q_i (A from tensor memory;
                 // 16 queries = 8 packed columns of A, 16 rows of B per step).
-                // Queries 16 m .. 16 m + 15 of the half have P^T at columns
-                // 16 m .. + 7 and dS^T at 16 m + 8 .. + 15 of S^T buffer h.
+                // Queries 16 m .. 16 m + 15 have P^T at columns 16 m .. + 7 and
+                // dS^T at 16 m + 8 .. + 15 (see the softmax warps).
 #pragma unroll
-                for (int kk = 0; kk < kHQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDV, tmem + kColS + h * kHQ + kk * 16, sdesc_advance(dom_desc, kk * 2048),
-                               idesc_acc, kk > 0 ? 1u : acc_first);
+                for (int kk = 0; kk < kBQ / 16; ++kk)
+                    mma_f16_ts(tmem + kColDV, tmem + kColS + kk * 16, sdesc_advance(dom_desc, kk * 2048), idesc_acc,
+                               kk > 0 ? 1u : acc_first);
 #pragma unroll
-                for (int kk = 0; kk < kHQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDK, tmem + kColS + h * kHQ + kk * 16 + 8, sdesc_advance(qm_desc, kk * 2048),
+                for (int kk = 0; kk < kBQ / 16; ++kk)
+                    mma_f16_ts(tmem + kColDK, tmem + kColS + kk * 16 + 8, sdesc_advance(qm_desc, kk * 2048),
                                idesc_acc, kk > 0 ? 1u : acc_first);
-                // both halves of the Q/dO tile are consumed once these complete
-                if (h == 1) mma_commit(&qd_empty[st]);
+                mma_commit(&qd_empty[st]);
+                if (it + 1 < n_it) {
+                    // S^T / dP^T of the next tile overwrite P^T, dS^T (read by the MMAs
+                    // just issued, which run first) and dQ^T (read out once dq_free flips)
+                    if constexpr (DQ) {
+                        if (!mbar_wait(dq_free, it & 1, abort_flag, p.status, 25)) { ok = false; break; }
+                    }
+                    tc_fence_after();
+                    if (!issue_sdp(it + 1)) { ok = false; break; }
+                }
             }
             if (ok) mma_commit(acc_done);
             // every MMA issued above has completed once `drain` flips
@@ -353,9 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp < 8) {
         // ----------------------------------- warps 0-7: softmax (P^T, dS^T)
-        // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and,
-        // of every 64-query half-tile, the query columns 32 hf .. + 31
-        // (hf = w / 4) in two chunks of 16.
+        // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
+        // query columns 64 hf .. + 63 (hf = w / 4), in four chunks of 16.
         const int hf = warp >> 2;
         const int quarter = warp & 3;
         const int c = quarter * 32 + lane;  // key row == TMEM lane
@@ -366,33 +343,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         // score 0 is not covered by L, and exp(0 - L) can overflow
         const bool kv_oob = kv >= N;
         bool ok = true;
-        for (int u = 0; u < n_u; ++u) {
-            const int h = u & 1;
-            const int it = u >> 1;
+        for (int it = 0; it < n_it; ++it) {
             const int st = it % QS;
             // every lane waits, then the warp votes: the tcgen05.ld/st below
             // are warp-collective and need all 32 lanes
-            const bool w1 = mbar_wait(&sdp_full[h], (u >> 1) & 1, abort_flag, p.status, 26);
+            const bool w1 = mbar_wait(sdp_full, it & 1, abort_flag, p.status, 26);
             const bool w2 = w1 && mbar_wait(&qd_full[st], (it / QS) & 1, abort_flag, p.status, 27);
             if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
             tc_fence_after();
             const int q_base = (i_start + it % n_i) * kBQ;
-            const int qs0 = h * kHQ + hf * 32;  // first query (in the Q tile) of this warp's slice
-            const bool diag = p.causal && (q_base + qs0 < kv0 + kBKV);
-            // some query of this slice is W or more rows below some key of the tile
-            const bool wmask = win > 0 && (q_base + qs0 + 31 - kv0 >= win);
-            uint8_t *ds_row = smem + L::OFF_DS + h * L::DS_BOX + c * 128;
-            // both chunks of S^T and dP^T in one round trip
-            uint32_t sv[32], dpv[32];
-            tmem_ld_x32(lane_base + kColS + qs0, sv);
-            tmem_ld_x32(lane_base + kColDP + qs0, dpv);
-            tmem_ld_wait_x32(sv);
-            tmem_ld_wait_x32(dpv);
+            const bool diag = p.causal && (q_base + hf * 64 < kv0 + kBKV);
+            // some query of this half is W or more rows below some key of the tile
+            const bool wmask = win > 0 && (q_base + hf * 64 + 63 - kv0 >= win);
+            uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const int qc = qs0 + ch * 16;  // first query column (in the Q tile) of this chunk
-                const uint32_t *s = sv + 16 * ch;
-                const uint32_t *dp = dpv + 16 * ch;
+            // S^T and dP^T of chunk ch + 1 load while chunk ch is computed
+            // (two register buffers; a wait covers every load issued so far)
+            uint32_t sbuf[2][16], dbuf[2][16];
+            tmem_ld_x16(lane_base + kColS + hf * 64, sbuf[0]);
+            tmem_ld_x16(lane_base + kColDP + hf * 64, dbuf[0]);
+            tmem_ld_wait_x16(sbuf[0]);
+            tmem_ld_wait_x16(dbuf[0]);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const int qc = hf * 64 + ch * 16;  // first query column of this chunk
+                uint32_t *s = sbuf[ch & 1];
+                uint32_t *dp = dbuf[ch & 1];
+                if (ch < 3) {
+                    tmem_ld_x16(lane_base + kColS + qc + 16, sbuf[(ch + 1) & 1]);
+                    tmem_ld_x16(lane_base + kColDP + qc + 16, dbuf[(ch + 1) & 1]);
+                }
                 const float *nl2 = ld_smem + st * 2 * kBQ + qc;          // -L log2(e)
                 const float *dsm = ld_smem + st * 2 * kBQ + kBQ + qc;    // D
                 const int q_first = q_base + qc;
@@ -431,25 +411,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 // P^T and dS^T of this chunk go into the chunk's own S^T columns
-                // of buffer h, which this warp has just read and no other warp
-                // reads: P^T at the first 8 of its 16 columns, dS^T at the last 8
-                const uint32_t col = kColS + h * kHQ + (qc - h * kHQ);
-                tmem_st_x8(lane_base + col, pp);
-                tmem_st_x8(lane_base + col + 8, dd);
+                // [qc, qc + 16), which this warp has just read and no other warp
+                // reads: P^T at qc .. qc + 7, dS^T at qc + 8 .. qc + 15
+                tmem_st_x8(lane_base + kColS + qc, pp);
+                tmem_st_x8(lane_base + kColS + qc + 8, dd);
                 if constexpr (DQ) {
-                    // dS^T row c of box h, the chunk's 16 queries -> 16-byte chunks
-                    // (qc - 64 h) / 8 and the next of the 128-byte swizzled row
-                    const int k0 = (qc - h * kHQ) >> 3;
+                    // dS^T row c, queries qc .. qc + 15 -> 16-byte chunks 2 ch, 2 ch + 1
+                    // of the 128-byte swizzled row of box hf
 #pragma unroll
                     for (int q = 0; q < 2; ++q)
-                        *reinterpret_cast<uint4 *>(ds_row + (((k0 + q) ^ (c & 7)) << 4)) =
+                        *reinterpret_cast<uint4 *>(ds_row + (((2 * ch + q) ^ (c & 7)) << 4)) =
                             make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
+                }
+                if (ch < 3) {
+                    tmem_ld_wait_x16(sbuf[(ch + 1) & 1]);
+                    tmem_ld_wait_x16(dbuf[(ch + 1) & 1]);
                 }
             }
             if constexpr (DQ) fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&ds_ready[h]);
+            mbar_arrive(ds_ready);
         }
         // ------------------------------- epilogue: dV (warps 0-3), dK (warps 4-7)
         bool ok2 = ok && mbar_wait(acc_done, 0, abort_flag, p.status, 28);
@@ -508,28 +490,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------- warps 8-15: dQ^T read-out and atomic reduction
-        // Warps 8-11 take the half-tiles of buffer 0, warps 12-15 those of
-        // buffer 1; warp w reads TMEM lane quarter w % 4 (lane = head-dim index
-        // t) and the 64 query columns of the half-tile.
-        const int hb = (warp - 8) >> 2;
+        // Warp w reads TMEM lane quarter w % 4 (lane = head-dim index t) and
+        // query columns 64 hf .. + 63 (hf = (w - 8) / 4).
+        const int hf = (warp - 8) >> 2;
         const int quarter = warp & 3;
         const int t = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        for (int u = hb; DQ && u < n_u; u += 2) {
-            const bool got = mbar_wait(&dq_full[hb], (u >> 1) & 1, abort_flag, p.status, 29);
+        for (int it = 0; DQ && it < n_it; ++it) {
+            const bool got = mbar_wait(dq_full, it & 1, abort_flag, p.status, 29);
             if (!__all_sync(0xffffffffu, got)) break;
             tc_fence_after();
             uint32_t v[64];
-            tmem_ld_x32(lane_base + kColDQ + hb * kHQ, v);
-            tmem_ld_x32(lane_base + kColDQ + hb * kHQ + 32, v + 32);
+            tmem_ld_x32(lane_base + kColDQ + hf * 64, v);
+            tmem_ld_x32(lane_base + kColDQ + hf * 64 + 32, v + 32);
             tmem_ld_wait_x32(v);
             tmem_ld_wait_x32(v + 32);
             tc_fence_before();
-            mbar_arrive(&dq_free[hb]);
-            const int it = u >> 1;
+            mbar_arrive(dq_free);
             const int h = g * G + it / n_i;
-            const int q_first = (i_start + it % n_i) * kBQ + hb * kHQ;
-            const int rows = min(kHQ, N - q_first);
+            const int q_first = (i_start + it % n_i) * kBQ + hf * 64;
+            const int rows = min(64, N - q_first);
             if (t < D) {
                 // element (q, t) of this head's dQ: consecutive lanes touch
                 // consecutive floats (one 128-byte line per warp and row)
