@@ -95,21 +95,21 @@ __device__ __forceinline__ void hadamard_row(float (&x)[8], int sub) {
     for (int i = 0; i < 8; ++i) x[i] *= inv_sqrt_d;
 }
 
+// Loads one 16-byte slice (8 values) of `row`, or zeros past the end.
 template <int D>
-__device__ __forceinline__ void load_rotated(const uint4 *__restrict__ x, const float *__restrict__ signs, long row,
-                                             long rows, int sub, float (&v)[8]) {
-    if (row < rows) {
-        const uint4 u = x[row * (D / 8) + sub];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ uint4 load_slice(const uint4 *__restrict__ x, long row, long rows, int sub) {
+    return row < rows ? x[row * (D / 8) + sub] : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Widens a slice to floats, applies the signs and the row transform.
+template <int D>
+__device__ __forceinline__ void rotate_slice(uint4 u, const float *__restrict__ signs, int sub, float (&v)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = unpack2<true>(w[i]);
-            v[2 * i] = f.x;
-            v[2 * i + 1] = f.y;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack2<true>(w[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
     }
     if (signs) {
 #pragma unroll
@@ -119,6 +119,10 @@ __device__ __forceinline__ void load_rotated(const uint4 *__restrict__ x, const 
 }
 
 __global__ void hq_zero_kernel(float *amax) { *amax = 0.0f; }
+
+// Each warp takes kU groups of rows per trip and issues all their loads before
+// transforming any, so several loads per warp are in flight.
+constexpr int kU = 4;
 
 template <int D>
 __global__ void __launch_bounds__(256) hq_amax_kernel(const uint4 *__restrict__ x, const float *__restrict__ signs,
@@ -131,11 +135,17 @@ __global__ void __launch_bounds__(256) hq_amax_kernel(const uint4 *__restrict__ 
     const int sub = lane % LPR;
     float m = 0.0f;
     // warp-uniform trip count: the shuffles inside need every lane
-    for (long base = warp_id * RPW; base < rows; base += nwarps * RPW) {
-        float v[8];
-        load_rotated<D>(x, signs, base + lane / LPR, rows, sub, v);
+    for (long base = warp_id * RPW * kU; base < rows; base += nwarps * RPW * kU) {
+        uint4 u[kU];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+        for (int k = 0; k < kU; ++k) u[k] = load_slice<D>(x, base + k * RPW + lane / LPR, rows, sub);
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+            float v[8];
+            rotate_slice<D>(u[k], signs, sub, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+        }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -163,14 +173,20 @@ __global__ void __launch_bounds__(256) hq_quant_kernel(const uint4 *__restrict__
     const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int sub = lane % LPR;
-    for (long base = warp_id * RPW; base < rows; base += nwarps * RPW) {
-        const long row = base + lane / LPR;
-        float v[8];
-        load_rotated<D>(x, signs, row, rows, sub, v);
-        if (row < rows) {
-            const uint32_t lo = cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
-            const uint32_t hi = cvt_e4m3x2(v[4] * inv, v[5] * inv) | (cvt_e4m3x2(v[6] * inv, v[7] * inv) << 16);
-            x8[row * (D / 8) + sub] = make_uint2(lo, hi);
+    for (long base = warp_id * RPW * kU; base < rows; base += nwarps * RPW * kU) {
+        uint4 u[kU];
+#pragma unroll
+        for (int k = 0; k < kU; ++k) u[k] = load_slice<D>(x, base + k * RPW + lane / LPR, rows, sub);
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+            const long row = base + k * RPW + lane / LPR;
+            float v[8];
+            rotate_slice<D>(u[k], signs, sub, v);
+            if (row < rows) {
+                const uint32_t lo = cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
+                const uint32_t hi = cvt_e4m3x2(v[4] * inv, v[5] * inv) | (cvt_e4m3x2(v[6] * inv, v[7] * inv) << 16);
+                x8[row * (D / 8) + sub] = make_uint2(lo, hi);
+            }
         }
     }
 }
