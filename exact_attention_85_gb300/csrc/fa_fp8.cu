@@ -122,7 +122,7 @@ __global__ void hq_zero_kernel(float *amax) { *amax = 0.0f; }
 
 // Each warp takes kU groups of rows per trip and issues all their loads before
 // transforming any, so several loads per warp are in flight.
-constexpr int kU = 4;
+constexpr int kU = 8;
 
 template <int D>
 __global__ void __launch_bounds__(256) hq_amax_kernel(const uint4 *__restrict__ x, const float *__restrict__ signs,
