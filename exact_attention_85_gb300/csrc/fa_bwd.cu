@@ -66,9 +66,9 @@ struct BwdLayout {
     static constexpr int OFF_DS = OFF_QD + QS * 2 * TILE_Q;
     static constexpr int OFF_LD = OFF_DS + DS_BYTES;  // stage s: L2[128], D[128]
     static constexpr int OFF_BAR = OFF_LD + QS * 2 * kBQ * 4;
-    // kv_full, qd_full[QS], qd_empty[QS], sdp_full, ds_ready, dq_full, dq_free,
-    // acc_done, drain
-    static constexpr int NBAR = 1 + 2 * QS + 4 + 2;
+    // kv_full, qd_full[QS], qd_empty[QS], s_full, dp_full, p_ready, ds_ready,
+    // dq_full, dq_free, acc_done, drain
+    static constexpr int NBAR = 1 + 2 * QS + 6 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SLACK = 512;  // room to align the dynamic shared base up to 1024
@@ -115,8 +115,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *kv_full = bars;
     uint64_t *qd_full = bars + 1;
     uint64_t *qd_empty = qd_full + QS;
-    uint64_t *sdp_full = qd_empty + QS;
-    uint64_t *ds_ready = sdp_full + 1;
+    uint64_t *s_full = qd_empty + QS;
+    uint64_t *dp_full = s_full + 1;
+    uint64_t *p_ready = dp_full + 1;
+    uint64_t *ds_ready = p_ready + 1;
     uint64_t *dq_full = ds_ready + 1;
     uint64_t *dq_free = dq_full + 1;
     uint64_t *acc_done = dq_free + 1;
@@ -164,7 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&qd_full[s], 33);
             mbar_init(&qd_empty[s], 1);
         }
-        mbar_init(sdp_full, 1);
+        mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(p_ready, kSoftmaxThreads);
         mbar_init(ds_ready, kSoftmaxThreads);
         mbar_init(dq_full, 1);
         mbar_init(dq_free, kReadoutThreads);
@@ -258,7 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kStage = 2 * L::TILE_Q;  // bytes between Q/dO stages
             bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 22);
 
-            // S^T = K_j Q_t^T -> [0, 128) and dP^T = V_j dO_t^T -> [128, 256)
+            // S^T = K_j Q_t^T -> [0, 128) (commit s_full), then dP^T = V_j dO_t^T
+            // -> [128, 256) (commit dp_full): the softmax warps start on P^T as
+            // soon as S^T is there, while the tensor cores compute dP^T
             auto issue_sdp = [&](int t) -> bool {
                 const int st = t % QS;
                 if (!mbar_wait(&qd_full[st], (t / QS) & 1, abort_flag, p.status, 23)) return false;
@@ -272,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f16_ss(tmem + kColS, sdesc_advance(k_desc, okv), sdesc_advance(q_desc, oq), idesc_sdp,
                                kk > 0 ? 1u : 0u);
                 }
+                mma_commit(s_full);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
@@ -279,13 +286,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f16_ss(tmem + kColDP, sdesc_advance(v_desc, okv), sdesc_advance(do_desc, oq), idesc_sdp,
                                kk > 0 ? 1u : 0u);
                 }
-                mma_commit(sdp_full);
+                mma_commit(dp_full);
                 return true;
             };
 
             if (ok) ok = issue_sdp(0);
             for (int it = 0; ok && it < n_it; ++it) {
                 const int st = it % QS;
+                const uint64_t qm_desc = sdesc_advance(qm_desc0, st * kStage);
+                const uint64_t dom_desc = sdesc_advance(dom_desc0, st * kStage);
+                const uint32_t acc_first = it > 0 ? 1u : 0u;
+                // dV_j += P^T dO_i as soon as P^T is written (the softmax warps
+                // compute dS^T meanwhile).  A from tensor memory: 16 queries = 8
+                // packed columns per step; queries 16 m .. 16 m + 15 have P^T at
+                // columns 16 m .. + 7 and dS^T at 16 m + 8 .. + 15.
+                if (!mbar_wait(p_ready, it & 1, abort_flag, p.status, 30)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kBQ / 16; ++kk)
+                    mma_f16_ts(tmem + kColDV, tmem + kColS + kk * 16, sdesc_advance(dom_desc, kk * 2048), idesc_acc,
+                               kk > 0 ? 1u : acc_first);
                 if (!mbar_wait(ds_ready, it & 1, abort_flag, p.status, 24)) { ok = false; break; }
                 tc_fence_after();
                 // dQ_i^T = K_j^T dS_i^T -> [128, 256) (lane = head-dim index);
@@ -297,17 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    sdesc_advance(ds_desc, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
                     mma_commit(dq_full);
                 }
-                const uint64_t qm_desc = sdesc_advance(qm_desc0, st * kStage);
-                const uint64_t dom_desc = sdesc_advance(dom_desc0, st * kStage);
-                const uint32_t acc_first = it > 0 ? 1u : 0u;
-                // dV_j += P^T dO_i and dK_j += dS^T Q_i (A from tensor memory;
-                // 16 queries = 8 packed columns of A, 16 rows of B per step).
-                // Queries 16 m .. 16 m + 15 have P^T at columns 16 m .. + 7 and
-                // dS^T at 16 m + 8 .. + 15 (see the softmax warps).
-#pragma unroll
-                for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDV, tmem + kColS + kk * 16, sdesc_advance(dom_desc, kk * 2048), idesc_acc,
-                               kk > 0 ? 1u : acc_first);
+                // dK_j += dS^T Q_i (A from tensor memory, as for dV)
 #pragma unroll
                 for (int kk = 0; kk < kBQ / 16; ++kk)
                     mma_f16_ts(tmem + kColDK, tmem + kColS + kk * 16 + 8, sdesc_advance(qm_desc, kk * 2048),
@@ -333,6 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ----------------------------------- warps 0-7: softmax (P^T, dS^T)
         // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
         // query columns 64 hf .. + 63 (hf = w / 4), in four chunks of 16.
+        // Two phases per Q tile: P^T from S^T (then p_ready, so dV += P^T dO
+        // runs), then dS^T = P^T o (dP^T - D) once dP^T is there (ds_ready).
         const int hf = warp >> 2;
         const int quarter = warp & 3;
         const int c = quarter * 32 + lane;  // key row == TMEM lane
@@ -347,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = it % QS;
             // every lane waits, then the warp votes: the tcgen05.ld/st below
             // are warp-collective and need all 32 lanes
-            const bool w1 = mbar_wait(sdp_full, it & 1, abort_flag, p.status, 26);
+            const bool w1 = mbar_wait(s_full, it & 1, abort_flag, p.status, 26);
             const bool w2 = w1 && mbar_wait(&qd_full[st], (it / QS) & 1, abort_flag, p.status, 27);
             if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
             tc_fence_after();
@@ -355,32 +367,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool diag = p.causal && (q_base + hf * 64 < kv0 + kBKV);
             // some query of this half is W or more rows below some key of the tile
             const bool wmask = win > 0 && (q_base + hf * 64 + 63 - kv0 >= win);
-            uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
-#pragma unroll
-            // S^T and dP^T of chunk ch + 1 load while chunk ch is computed
-            // (two register buffers; a wait covers every load issued so far)
-            uint32_t sbuf[2][16], dbuf[2][16];
-            tmem_ld_x16(lane_base + kColS + hf * 64, sbuf[0]);
-            tmem_ld_x16(lane_base + kColDP + hf * 64, dbuf[0]);
-            tmem_ld_wait_x16(sbuf[0]);
-            tmem_ld_wait_x16(dbuf[0]);
+            const float *ldst = ld_smem + st * 2 * kBQ;  // -L log2(e) [128], then D [128]
+            // ---- phase 1: P^T (16-bit pairs), kept in registers for phase 2
+            uint32_t pp[4][8];
+            uint32_t sv[32];  // S^T of two chunks at a time
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 const int qc = hf * 64 + ch * 16;  // first query column of this chunk
-                uint32_t *s = sbuf[ch & 1];
-                uint32_t *dp = dbuf[ch & 1];
-                if (ch < 3) {
-                    tmem_ld_x16(lane_base + kColS + qc + 16, sbuf[(ch + 1) & 1]);
-                    tmem_ld_x16(lane_base + kColDP + qc + 16, dbuf[(ch + 1) & 1]);
-                }
-                const float *nl2 = ld_smem + st * 2 * kBQ + qc;          // -L log2(e)
-                const float *dsm = ld_smem + st * 2 * kBQ + kBQ + qc;    // D
                 const int q_first = q_base + qc;
-                uint32_t pp[8], dd[8];
+                if ((ch & 1) == 0) {
+                    tmem_ld_x32(lane_base + kColS + qc, sv);
+                    tmem_ld_wait_x32(sv);
+                }
+                const uint32_t *s = sv + 16 * (ch & 1);
 #pragma unroll
                 for (int r = 0; r < 16; r += 2) {
                     const float2 x = ffma2(make_float2(__uint_as_float(s[r]), __uint_as_float(s[r + 1])), sl2,
-                                           *reinterpret_cast<const float2 *>(nl2 + r));
+                                           *reinterpret_cast<const float2 *>(ldst + qc + r));
                     float p0 = ex2_approx(x.x);
                     float p1 = ex2_approx(x.y);
                     if (diag) {  // causal: key kv is visible to query q iff kv <= q
@@ -391,29 +394,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (q_first + r - kv >= win) p0 = 0.0f;
                         if (q_first + r + 1 - kv >= win) p1 = 0.0f;
                     }
-                    const float2 t = fsub2(make_float2(__uint_as_float(dp[r]), __uint_as_float(dp[r + 1])),
-                                           *reinterpret_cast<const float2 *>(dsm + r));
-                    const float2 ds = fmul2(make_float2(p0, p1), t);
-                    if constexpr (BF16) {
-                        pp[r / 2] = pack_bf16x2(p0, p1);
-                        dd[r / 2] = pack_bf16x2(ds.x, ds.y);
-                    } else {
-                        pp[r / 2] = pack_f16x2(p0, p1);
-                        dd[r / 2] = pack_f16x2(ds.x, ds.y);
-                    }
+                    pp[ch][r / 2] = BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
                 }
                 if (kv_oob) {  // P = 0, hence dS = 0, for the whole row
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        pp[r] = 0u;
-                        dd[r] = 0u;
-                    }
+                    for (int r = 0; r < 8; ++r) pp[ch][r] = 0u;
                 }
                 __syncwarp();
-                // P^T and dS^T of this chunk go into the chunk's own S^T columns
-                // [qc, qc + 16), which this warp has just read and no other warp
-                // reads: P^T at qc .. qc + 7, dS^T at qc + 8 .. qc + 15
-                tmem_st_x8(lane_base + kColS + qc, pp);
+                // P^T of this chunk goes into the first 8 of the chunk's own S^T
+                // columns [qc, qc + 16), which this warp has read and no other reads
+                tmem_st_x8(lane_base + kColS + qc, pp[ch]);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(p_ready);
+            // ---- phase 2: dS^T = P^T o (dP^T - D), from the rounded P^T above
+            const bool w3 = mbar_wait(dp_full, it & 1, abort_flag, p.status, 31);
+            if (!__all_sync(0xffffffffu, w3)) { ok = false; break; }
+            tc_fence_after();
+            uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
+            uint32_t dpv[32];  // dP^T of two chunks at a time
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const int qc = hf * 64 + ch * 16;
+                if ((ch & 1) == 0) {
+                    tmem_ld_x32(lane_base + kColDP + qc, dpv);
+                    tmem_ld_wait_x32(dpv);
+                }
+                const uint32_t *dp = dpv + 16 * (ch & 1);
+                uint32_t dd[8];
+#pragma unroll
+                for (int r = 0; r < 16; r += 2) {
+                    const float2 pv = unpack2<BF16>(pp[ch][r / 2]);
+                    const float2 t = fsub2(make_float2(__uint_as_float(dp[r]), __uint_as_float(dp[r + 1])),
+                                           *reinterpret_cast<const float2 *>(ldst + kBQ + qc + r));
+                    const float2 ds = fmul2(pv, t);
+                    dd[r / 2] = BF16 ? pack_bf16x2(ds.x, ds.y) : pack_f16x2(ds.x, ds.y);
+                }
+                __syncwarp();
+                // dS^T into the last 8 of the chunk's 16 S^T columns
                 tmem_st_x8(lane_base + kColS + qc + 8, dd);
                 if constexpr (DQ) {
                     // dS^T row c, queries qc .. qc + 15 -> 16-byte chunks 2 ch, 2 ch + 1
@@ -422,10 +441,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q = 0; q < 2; ++q)
                         *reinterpret_cast<uint4 *>(ds_row + (((2 * ch + q) ^ (c & 7)) << 4)) =
                             make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
-                }
-                if (ch < 3) {
-                    tmem_ld_wait_x16(sbuf[(ch + 1) & 1]);
-                    tmem_ld_wait_x16(dbuf[(ch + 1) & 1]);
                 }
             }
             if constexpr (DQ) fence_proxy_async_smem();
