@@ -912,7 +912,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                         if (kv > kv_last || kv < kv_lo) p0 = 0.0f;
                         if (kv + 1 > kv_last || kv + 1 < kv_lo) p1 = 0.0f;
                     }
-                    const float2 ds = fmul2(make_float2(p0, p1),
+                    // P rounded to the element type, as in the K/V-tile pass (where
+                    // the same rounded P feeds dV), so both passes use one dS
+                    const float2 pr = unpack2<BF16>(BF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1));
+                    const float2 ds = fmul2(pr,
                                             fsub2(make_float2(__uint_as_float(dp[32 * c + x]),
                                                               __uint_as_float(dp[32 * c + x + 1])),
                                                   dx2));
