@@ -380,10 +380,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait_x32(sv);
                 }
                 const uint32_t *s = sv + 16 * (ch & 1);
+                // the chunk's 16 values of -L log2(e) in four 16-byte loads
+                float nl[16];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 f = *reinterpret_cast<const float4 *>(ldst + qc + 4 * k);
+                    nl[4 * k] = f.x;
+                    nl[4 * k + 1] = f.y;
+                    nl[4 * k + 2] = f.z;
+                    nl[4 * k + 3] = f.w;
+                }
 #pragma unroll
                 for (int r = 0; r < 16; r += 2) {
                     const float2 x = ffma2(make_float2(__uint_as_float(s[r]), __uint_as_float(s[r + 1])), sl2,
-                                           *reinterpret_cast<const float2 *>(ldst + qc + r));
+                                           make_float2(nl[r], nl[r + 1]));
                     float p0 = ex2_approx(x.x);
                     float p1 = ex2_approx(x.y);
                     if (diag) {  // causal: key kv is visible to query q iff kv <= q
@@ -422,12 +432,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait_x32(dpv);
                 }
                 const uint32_t *dp = dpv + 16 * (ch & 1);
+                float dv_[16];  // the chunk's 16 values of D
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float4 f = *reinterpret_cast<const float4 *>(ldst + kBQ + qc + 4 * k);
+                    dv_[4 * k] = f.x;
+                    dv_[4 * k + 1] = f.y;
+                    dv_[4 * k + 2] = f.z;
+                    dv_[4 * k + 3] = f.w;
+                }
                 uint32_t dd[8];
 #pragma unroll
                 for (int r = 0; r < 16; r += 2) {
                     const float2 pv = unpack2<BF16>(pp[ch][r / 2]);
                     const float2 t = fsub2(make_float2(__uint_as_float(dp[r]), __uint_as_float(dp[r + 1])),
-                                           *reinterpret_cast<const float2 *>(ldst + kBQ + qc + r));
+                                           make_float2(dv_[r], dv_[r + 1]));
                     const float2 ds = fmul2(pv, t);
                     dd[r / 2] = BF16 ? pack_bf16x2(ds.x, ds.y) : pack_f16x2(ds.x, ds.y);
                 }
