@@ -29,11 +29,12 @@
 //   [256, 256 + d) dV_j,  [384, 384 + d) dK_j  (accumulated over all Q tiles)
 // P^T and dS^T stay in tensor memory as the A operands of dV += P^T dO and
 // dK += dS^T Q; dS^T is also written to shared memory as the B operand of
-// dQ^T = K^T dS^T.  Per Q tile: MMA S^T, dP^T -> softmax warps -> MMA dQ^T,
-// dV, dK -> read-out warps copy dQ^T out of tensor memory (which frees the
-// columns for the next S^T, dP^T) and add it into dQacc with fp32 atomic
-// reductions (one 128-byte line per warp and query row) while the softmax
-// warps already work on the next tile.
+// dQ^T = K^T dS^T.  Per Q tile: MMA S^T -> softmax phase 1 (P^T) while the
+// tensor cores compute dP^T -> MMA dV += P^T dO while softmax phase 2 forms
+// dS^T -> MMA dQ^T, dK -> read-out warps copy dQ^T out of tensor memory
+// (which frees the columns for the next S^T, dP^T) and add it into dQacc
+// with fp32 atomic reductions (one 128-byte line per warp and query row)
+// while the softmax warps already work on the next tile.
 // Warps: 0-7 softmax (then 0-3 store dV, 4-7 store dK), 8-15 dQ read-out,
 // 16 TMA producer (Q / dO through a 2-deep ring), 17 MMA issuer + TMEM owner.
 #include "host_util.h"
@@ -342,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < 8) {
         // ----------------------------------- warps 0-7: softmax (P^T, dS^T)
         // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
-        // query columns 64 hf .. + 63 (hf = w / 4), in four chunks of 16.
+        // query columns 64 hf .. + 63 (hf = w / 4), in four chunks of 16 (two
+        // per tensor-memory load).
         // Two phases per Q tile: P^T from S^T (then p_ready, so dV += P^T dO
         // runs), then dS^T = P^T o (dP^T - D) once dP^T is there (ds_ready).
         const int hf = warp >> 2;
