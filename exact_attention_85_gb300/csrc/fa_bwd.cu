@@ -132,6 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int win = GENERAL ? p.window : 0;
     const bool packed = GENERAL && p.varlen;
+    // without the dQ part the read-out warps 8-15 join the softmax: 16 warps,
+    // 32 query columns each instead of 8 warps of 64
+    constexpr int kSmWarps = DQ ? 8 : 16;
+    constexpr int kNCH = DQ ? 4 : 2;  // 16-query chunks per softmax warp
 
     const int bg = blockIdx.x / p.nkv;  // batch * Hkv + g
     const int jt = blockIdx.x - bg * p.nkv;
@@ -169,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
-        mbar_init(p_ready, kSoftmaxThreads);
-        mbar_init(ds_ready, kSoftmaxThreads);
+        mbar_init(p_ready, kSmWarps * 32);
+        mbar_init(ds_ready, kSmWarps * 32);
         mbar_init(dq_full, 1);
         mbar_init(dq_free, kReadoutThreads);
         mbar_init(acc_done, 1);
@@ -340,14 +344,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_drain(drain, 0, 100000000ull);
         }
         __syncwarp();
-    } else if (warp < 8) {
-        // ----------------------------------- warps 0-7: softmax (P^T, dS^T)
+    } else if (warp < kSmWarps) {
+        // -------------------- warps 0-7 (0-15 without dQ): softmax (P^T, dS^T)
         // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quarter) and
-        // query columns 64 hf .. + 63 (hf = w / 4), in four chunks of 16 (two
-        // per tensor-memory load).
+        // query columns q0w .. q0w + 16 kNCH - 1 (q0w = 16 kNCH (w / 4)), in
+        // chunks of 16 (two per tensor-memory load).
         // Two phases per Q tile: P^T from S^T (then p_ready, so dV += P^T dO
         // runs), then dS^T = P^T o (dP^T - D) once dP^T is there (ds_ready).
-        const int hf = warp >> 2;
+        const int hf = warp >> 2;  // query slice; dV (0) or dK (1) in the epilogue
+        const int q0w = hf * 16 * kNCH;
         const int quarter = warp & 3;
         const int c = quarter * 32 + lane;  // key row == TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
@@ -366,16 +371,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
             tc_fence_after();
             const int q_base = (i_start + it % n_i) * kBQ;
-            const bool diag = p.causal && (q_base + hf * 64 < kv0 + kBKV);
-            // some query of this half is W or more rows below some key of the tile
-            const bool wmask = win > 0 && (q_base + hf * 64 + 63 - kv0 >= win);
+            const bool diag = p.causal && (q_base + q0w < kv0 + kBKV);
+            // some query of this slice is W or more rows below some key of the tile
+            const bool wmask = win > 0 && (q_base + q0w + 16 * kNCH - 1 - kv0 >= win);
             const float *ldst = ld_smem + st * 2 * kBQ;  // -L log2(e) [128], then D [128]
             // ---- phase 1: P^T (16-bit pairs), kept in registers for phase 2
-            uint32_t pp[4][8];
+            uint32_t pp[kNCH][8];
             uint32_t sv[32];  // S^T of two chunks at a time
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                const int qc = hf * 64 + ch * 16;  // first query column of this chunk
+            for (int ch = 0; ch < kNCH; ++ch) {
+                const int qc = q0w + ch * 16;  // first query column of this chunk
                 const int q_first = q_base + qc;
                 if ((ch & 1) == 0) {
                     tmem_ld_x32(lane_base + kColS + qc, sv);
@@ -427,8 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
             uint32_t dpv[32];  // dP^T of two chunks at a time
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                const int qc = hf * 64 + ch * 16;
+            for (int ch = 0; ch < kNCH; ++ch) {
+                const int qc = q0w + ch * 16;
                 if ((ch & 1) == 0) {
                     tmem_ld_x32(lane_base + kColDP + qc, dpv);
                     tmem_ld_wait_x32(dpv);
@@ -470,9 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(ds_ready);
         }
         // ------------------------------- epilogue: dV (warps 0-3), dK (warps 4-7)
-        bool ok2 = ok && mbar_wait(acc_done, 0, abort_flag, p.status, 28);
+        bool ok2 = ok && warp < 8 && mbar_wait(acc_done, 0, abort_flag, p.status, 28);
         __syncwarp();
-        ok2 = named_bar_and(1 + hf, 128, ok2);
+        if (warp < 8) ok2 = named_bar_and(1 + hf, 128, ok2);  // uniform per warp group
         if (ok2) {
             tc_fence_after();
             // the first Q/dO stage is idle after the last MMA: dV goes to its Q
