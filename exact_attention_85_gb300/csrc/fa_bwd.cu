@@ -35,8 +35,9 @@
 // (which frees the columns for the next S^T, dP^T) and add it into dQacc
 // with fp32 atomic reductions (one 128-byte line per warp and query row)
 // while the softmax warps already work on the next tile.
-// Warps: 0-7 softmax (then 0-3 store dV, 4-7 store dK), 8-15 dQ read-out,
-// 16 TMA producer (Q / dO through a 2-deep ring), 17 MMA issuer + TMEM owner.
+// Warps: 0-7 softmax (then 0-3 store dV, 4-7 store dK), 8-15 dQ read-out
+// (softmax too when the kernel runs without its dQ part), 16 TMA producer
+// (Q / dO through a 2-deep ring), 17 MMA issuer + TMEM owner.
 #include "host_util.h"
 #include "ptx.cuh"
 
@@ -47,7 +48,6 @@ namespace {
 constexpr int kBQ = 128;       // query rows per Q tile
 constexpr int kBKV = 128;      // key rows per CTA (TMEM lanes)
 constexpr int kThreads = 576;  // 18 warps
-constexpr int kSoftmaxThreads = 256;  // warps 0-7
 constexpr int kReadoutThreads = 256;  // warps 8-15
 constexpr int kProducerWarp = 16, kMmaWarp = 17;
 
