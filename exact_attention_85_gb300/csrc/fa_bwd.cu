@@ -38,6 +38,7 @@
 // Warps: 0-7 softmax (then 0-3 store dV, 4-7 store dK), 8-15 dQ read-out
 // (softmax too when the kernel runs without its dQ part), 16 TMA producer
 // (Q / dO through a 2-deep ring), 17 MMA issuer + TMEM owner.
+#include "grid_order.cuh"
 #include "host_util.h"
 #include "ptx.cuh"
 
@@ -88,6 +89,7 @@ struct BwdParams {
     int Hq, Hkv, N, nkv, nq;
     int causal;
     int window;  // > 0: query r sees keys r - window + 1 .. r only
+    int group;   // key/value planes per CTA-order group (grid_order.cuh)
     float scale, scale_log2;
 };
 
@@ -137,8 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kSmWarps = DQ ? 8 : 16;
     constexpr int kNCH = DQ ? 4 : 2;  // 16-query chunks per softmax warp
 
-    const int bg = blockIdx.x / p.nkv;  // batch * Hkv + g
-    const int jt = blockIdx.x - bg * p.nkv;
+    // CTA order: key/value planes in L2-sized groups; the first K/V tiles of
+    // a causal plane visit the most Q tiles and go first
+    int bg, jt;  // bg = batch * Hkv + g
+    grid_decode(blockIdx.x, (int)(gridDim.x / p.nkv), p.nkv, p.group, bg, jt);
     const int b = bg / p.Hkv;
     const int g = bg - b * p.Hkv;
     const int G = p.Hq / p.Hkv;
@@ -697,6 +701,7 @@ struct DqParams {
     int Hq, Hkv, N, nq, nkv;
     int causal;
     int window;  // > 0: query r sees keys r - window + 1 .. r only
+    int group;   // query planes per CTA-order group (grid_order.cuh)
     float scale, scale_log2;
 };
 
@@ -733,10 +738,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int win = GENERAL ? p.window : 0;
     const bool packed = GENERAL && p.varlen;
 
-    // consecutive CTAs share a head (its K/V stay in L2); causal tiles go
-    // longest first within a head
-    const int bh = blockIdx.x / p.nq;
-    const int qt_lin = blockIdx.x - bh * p.nq;
+    // CTA order: query planes in L2-sized groups, longest causal tiles first
+    int bh, qt_lin;
+    grid_decode(blockIdx.x, (int)(gridDim.x / p.nq), p.nq, p.group, bh, qt_lin);
     const int qt = p.causal ? (p.nq - 1 - qt_lin) : qt_lin;
     const int b = bh / p.Hq;
     const int h = bh - b * p.Hq;
@@ -1072,6 +1076,13 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
     p.window = a.window;
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
+    int sms = 0;
+    {
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    }
+    p.group = grid_group_planes(a.B * a.Hkv, p.nkv, sms);
     const long long grid = (long long)p.nkv * a.B * a.Hkv;
     main_kernel<<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, tdo, tdk, tdv, p);
     e = cudaGetLastError();
@@ -1099,6 +1110,7 @@ cudaError_t launch_bwd_t(const BwdArgs &a, cudaStream_t st, bool two_pass) {
         pq2.window = a.window;
         pq2.scale = a.scale;
         pq2.scale_log2 = p.scale_log2;
+        pq2.group = grid_group_planes(a.B * a.Hq, p.nq, sms);
         const long long grid2 = (long long)p.nq * a.B * a.Hq;
         dq_kernel<<<dim3((unsigned)grid2), dim3(kDqThreads), LQ::ALLOC, st>>>(tq, tk, tv, tdo, tdq, pq2);
         return cudaGetLastError();

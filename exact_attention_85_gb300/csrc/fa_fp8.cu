@@ -24,6 +24,7 @@
 // tile's max exceeds it by more than 4 (log2 units), so P <= 2^8 < 448.  O is
 // normalised by the sum of the quantised P it was built from (the lift
 // cancels); L uses the sum of the unquantised P.
+#include "grid_order.cuh"
 #include "host_util.h"
 #include "ptx.cuh"
 
@@ -228,6 +229,7 @@ struct Fp8Params {
     const float *q_descale, *k_descale, *v_descale;
     unsigned int *status;
     int Hq, Hkv, N, nblk, causal;  // nblk: 256-row blocks per head
+    int group, planes;             // CTA order (grid_order.cuh): planes per group, B * Hq
     float scale_log2;
 };
 
@@ -255,9 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // consecutive CTAs share a head (K/V stay in L2); causal blocks longest first
-    const int bh = blockIdx.x / p.nblk;
-    const int t_lin = blockIdx.x - bh * p.nblk;
+    // CTA order: planes in L2-sized groups, longest causal blocks first
+    int bh, t_lin;
+    grid_decode(blockIdx.x, p.planes, p.nblk, p.group, bh, t_lin);
     const int t = p.causal ? (p.nblk - 1 - t_lin) : t_lin;
     const int b = bh / p.Hq;
     const int h = bh - b * p.Hq;
@@ -624,6 +626,13 @@ cudaError_t launch_fwd_fp8(const Fp8FwdArgs &a, cudaStream_t st) {
     p.Hkv = a.Hkv;
     p.N = a.N;
     p.nblk = (a.N + 2 * kBM - 1) / (2 * kBM);
+    {
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        p.planes = a.B * a.Hq;
+        p.group = grid_group_planes(p.planes, p.nblk, sms);
+    }
     p.causal = a.causal;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     const long long grid = (long long)p.nblk * a.B * a.Hq;

@@ -33,6 +33,7 @@
 // by 2^(m_ref_old - m_ref_new) once.  Between moves P = 2^(s - m_ref) <= 2^8,
 // and because O~ and l always share the same m_ref the final O~ / l is the
 // same quotient as with the page's per-tile update.
+#include "grid_order.cuh"
 #include "host_util.h"
 #include "ptx.cuh"
 
@@ -73,6 +74,7 @@ struct FwdParams {
     const int *cu_seqlens;         // packed layout: sequence b is rows cu[b] .. cu[b+1]-1
     int varlen, total;             // packed layout flag, rows of all sequences
     int Hq, Hkv, N, nblk, causal;  // N: rows per sequence (packed: the maximum); nblk: 256-row blocks
+    int group, planes;             // CTA order (grid_order.cuh): planes per group, B * Hq
     int window;                    // > 0: row r sees keys r - window + 1 .. r only
     float scale_log2;              // scale * log2(e)
 };
@@ -107,10 +109,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int win = GENERAL ? p.window : 0;
     const bool packed = GENERAL && p.varlen;
 
-    // Block schedule: consecutive CTAs share a head (K/V stay hot in L2);
-    // within a head, causal blocks go longest first.
-    const int bh = blockIdx.x / p.nblk;
-    const int t_lin = blockIdx.x - bh * p.nblk;
+    // CTA order: planes in L2-sized groups, longest causal blocks first
+    int bh, t_lin;
+    grid_decode(blockIdx.x, p.planes, p.nblk, p.group, bh, t_lin);
     const int t = p.causal ? (p.nblk - 1 - t_lin) : t_lin;
     const int b = bh / p.Hq;
     const int h = bh - b * p.Hq;
@@ -539,6 +540,13 @@ cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t st) {
     p.Hkv = a.Hkv;
     p.N = a.N;
     p.nblk = (a.N + 2 * kBM - 1) / (2 * kBM);
+    {
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        p.planes = a.B * a.Hq;
+        p.group = grid_group_planes(p.planes, p.nblk, sms);
+    }
     p.causal = a.causal;
     p.window = a.window;
     p.scale_log2 = a.scale * 1.4426950408889634f;
