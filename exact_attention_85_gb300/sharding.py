@@ -36,3 +36,37 @@ def query_heads(g: int, Hq: int, Hkv: int) -> range:
     """Query heads that read key/value head g (consecutive heads share one)."""
     G = Hq // Hkv
     return range(g * G, (g + 1) * G)
+
+
+def varlen_shard(cu_seqlens, world: int, rank: int):
+    """Packed batch (device-independent prefix sums `cu_seqlens` of B
+    sequences): the contiguous range of sequences owned by `rank`, chosen so
+    that the ranks' attention work is balanced (proportional to n^2 per
+    sequence, with or without the causal mask), and how to address it.
+
+    Returns (seq_lo, seq_hi, row_lo, row_hi, local_cu): the rank owns
+    sequences seq_lo .. seq_hi - 1, i.e. packed rows row_lo .. row_hi - 1, and
+    `local_cu` are their prefix sums relative to row_lo (pass the slices
+    [row_lo:row_hi] of the packed tensors and local_cu to the varlen entry
+    points).  Sequences are never split, so no exchange is needed."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad world size / rank")
+    cu = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+    lengths = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    work = [n * n for n in lengths]
+    total = sum(work)
+    # boundary r: first sequence whose cumulative work reaches r / world of the total
+    bounds = [0]
+    acc = 0
+    i = 0
+    for r in range(1, world):
+        target = total * r / world
+        while i < len(work) and acc + work[i] / 2 < target:
+            acc += work[i]
+            i += 1
+        bounds.append(max(i, bounds[-1]))
+    bounds.append(len(lengths))
+    lo, hi = bounds[rank], bounds[rank + 1]
+    row_lo, row_hi = cu[lo], cu[hi]
+    local_cu = [c - row_lo for c in cu[lo:hi + 1]]
+    return lo, hi, row_lo, row_hi, local_cu

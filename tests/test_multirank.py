@@ -90,3 +90,72 @@ def test_two_gloo_ranks_match_single_process(tmp_path):
     rq, rk, rv = oracle.attention_bwd(q, k, v, dO, True, 0.3)
     for got, ref in zip(res["outs"], (o_ref, rq, rk, rv)):
         np.testing.assert_allclose(got.numpy(), ref, atol=1e-12)
+
+
+# ----------------------------------------------- packed variable-length batch
+
+LENGTHS = [7, 0, 30, 3, 12, 25, 1]
+HQ_V, HKV_V, D_V = 4, 2, 8
+
+
+def _varlen_inputs():
+    g = torch.Generator().manual_seed(9)
+    total = sum(LENGTHS)
+    q = torch.randn(total, HQ_V, D_V, generator=g, dtype=torch.float64)
+    k = torch.randn(total, HKV_V, D_V, generator=g, dtype=torch.float64)
+    v = torch.randn(total, HKV_V, D_V, generator=g, dtype=torch.float64)
+    dO = torch.randn(total, HQ_V, D_V, generator=g, dtype=torch.float64)
+    cu = np.concatenate([[0], np.cumsum(LENGTHS)])
+    return q, k, v, dO, cu
+
+
+def _varlen_worker(rank, world, port, out_dir):
+    import oracle
+    from exact_attention_85_gb300.sharding import varlen_shard
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    q, k, v, dO, cu = _varlen_inputs()
+    _, _, r0, r1, lcu = varlen_shard(cu, world, rank)
+    outs = [torch.zeros_like(t) for t in (q, q, k, v)]
+    if r1 > r0:
+        # this rank's rows only, with offsets relative to its first row
+        o, _ = oracle.attention_fwd_varlen(q[r0:r1], k[r0:r1], v[r0:r1], lcu, True, 0.4)
+        gq, gk, gv = oracle.attention_bwd_varlen(q[r0:r1], k[r0:r1], v[r0:r1], dO[r0:r1], lcu, True, 0.4)
+        for t, val in zip(outs, (o, gq, gk, gv)):
+            t[r0:r1] = torch.from_numpy(val)
+    gathered = []
+    for t in outs:
+        parts = [torch.zeros_like(t) for _ in range(world)]
+        dist.all_gather(parts, t)
+        gathered.append(sum(parts))
+    if rank == 0:
+        torch.save(gathered, os.path.join(out_dir, "varlen.pt"))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_ranks_packed_batch_without_exchange(tmp_path):
+    import oracle
+    port = _free_port()
+    mp.spawn(_varlen_worker, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    got = torch.load(os.path.join(tmp_path, "varlen.pt"))
+    q, k, v, dO, cu = _varlen_inputs()
+    ro, _ = oracle.attention_fwd_varlen(q, k, v, cu, True, 0.4)
+    rq, rk, rv = oracle.attention_bwd_varlen(q, k, v, dO, cu, True, 0.4)
+    for t, ref in zip(got, (ro, rq, rk, rv)):
+        np.testing.assert_allclose(t.numpy(), ref, atol=1e-12)
+
+
+def test_varlen_shard_balances_and_covers():
+    from exact_attention_85_gb300.sharding import varlen_shard
+    cu = [0, 5, 5, 6, 15, 19, 1000, 1010]
+    for world in (1, 2, 3, 5):
+        spans = [varlen_shard(cu, world, r) for r in range(world)]
+        assert spans[0][0] == 0 and spans[-1][1] == len(cu) - 1
+        for a, b in zip(spans, spans[1:]):
+            assert a[1] == b[0] and a[3] == b[2]  # contiguous, no gaps or overlaps
+        for lo, hi, r0, r1, lcu in spans:
+            assert lcu == [c - r0 for c in cu[lo:hi + 1]] and r1 - r0 == lcu[-1]
+    # the long sequence gets a rank of its own
+    assert varlen_shard(cu, 2, 1)[:2] == (5, 7) or varlen_shard(cu, 2, 1)[:2] == (6, 7)
