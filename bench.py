@@ -251,7 +251,8 @@ def run_ours(a):
                    "causal": w.causal, "per_gpu_batch": w.B, "global_batch": w.B * ws,
                    "parallelism": f"dp{ws} (batch shards, no collective)",
                    "units_rank0": [u_lo, u_hi] if rank == 0 else None,
-                   "l2": "flushed between steps (256 MB write); inputs 537 MB also exceed L2",
+                   "l2": "flushed between steps (256 MB write); inputs 537 MB also exceed L2; "
+                         "l2_hot repeats the timing without the flush",
                    "backward_included": has_bwd},
         "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
         "fwd_tflops": round(fwd_tf, 1), "bwd_tflops": None if bwd_tf is None else round(bwd_tf, 1),
@@ -260,6 +261,9 @@ def run_ours(a):
         "roofline": roof, "gpu_launches": launches, "wall_s_timed": round(wall, 3),
         "clocks": clk.summary(),
     }
+
+    result["l2_hot"] = _hot_leg(a, fwd, bwd if has_bwd else None, stream, f_fwd, f_bwd)
+    result["exp2_bound"] = _exp2_leg(w, dev, stream, fwd_avg, bwd_avg if has_bwd else None)
 
     if has_bwd and not a.no_two_pass:
         result["two_pass_bwd_leg"] = _two_pass_leg(a, w, (q, k, v, o, lse, dO, dq, dk, dv), dev, stream, peaks,
@@ -278,6 +282,73 @@ def run_ours(a):
         print(json.dumps(result), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def _hot_leg(a, fwd, bwd, stream, f_fwd, f_bwd):
+    """The same calls back to back with no L2 flush between them (inputs
+    partly L2-resident from the previous call)."""
+    import torch
+
+    for _ in range(2):
+        fwd()
+        if bwd:
+            bwd()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    torch.cuda.synchronize()
+    for i in range(a.steps):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        if bwd:
+            bwd()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    fm = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    out = {"l2": "not flushed between steps", "fwd_ms": round(fm, 4),
+           "fwd_tflops": round(f_fwd / (fm * 1e-3) / 1e12, 1), "launches_per_step": 4 if bwd else 1}
+    if bwd:
+        bm = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        out.update(bwd_ms=round(bm, 4), bwd_tflops=round(f_bwd / (bm * 1e-3) / 1e12, 1))
+    return out
+
+
+def _visible_pairs(w) -> float:
+    """(query, key) pairs the mask lets through, over all heads and batches."""
+    per = w.N * (w.N + 1) / 2 if w.causal else w.N * w.N
+    return float(w.B * w.Hq * per)
+
+
+def _exp2_leg(w, dev, stream, fwd_ms, bwd_ms):
+    """exp2 throughput of the special-function unit (fa_probe_exp2) and the
+    time the forward / backward would take if bound by their exps alone:
+    one exp per visible score in the forward, one more per score in the
+    backward's recomputation of P."""
+    import torch
+    from exact_attention_85_gb300 import _lib
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = sms * 8, 2048
+    sink = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        n = _lib.fa_probe_exp2(sink, blocks, iters, stream)
+    times = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        n = _lib.fa_probe_exp2(sink, blocks, iters, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    rate = n / (ms * 1e-3)
+    exps = _visible_pairs(w)
+    out = {"probe": f"{blocks} blocks x 256 threads x 8 chains x {iters} ex2.approx.ftz.f32", "probe_ms": round(ms, 4),
+           "exp2_per_s": float(f"{rate:.4g}"), "exps_fwd": exps, "fwd_exp_bound_ms": round(exps / rate * 1e3, 4),
+           "fwd_exp_share": round(exps / rate * 1e3 / fwd_ms, 3), "launches": 8}
+    if bwd_ms:
+        out.update(exps_bwd=exps, bwd_exp_bound_ms=round(exps / rate * 1e3, 4),
+                   bwd_exp_share=round(exps / rate * 1e3 / bwd_ms, 3))
+    return out
 
 
 def _two_pass_leg(a, w, t, dev, stream, peaks, flush):
@@ -597,6 +668,27 @@ def _cpu_sample(w, host, n_groups: int):
     return secs, per_head * done
 
 
+def _cpu_single_thread_small():
+    """The oracle on one host thread, forward + backward of the whole small
+    fp16 workload (B1 H2 N256 d64, non-causal)."""
+    import oracle
+    from exact_attention_85_gb300.inputs import WORKLOADS, make_inputs
+
+    w1 = WORKLOADS["tiny_fp16_d64_n256"]
+    host1 = make_inputs(w1, with_grad=True)
+    oracle.set_threads(1)
+    try:
+        _cpu_sample(w1, host1, w1.B * w1.Hkv)  # warm-up (library load)
+        reps, secs, flops = 0, 0.0, 0.0
+        while secs < 1.0:
+            s1, f1 = _cpu_sample(w1, host1, w1.B * w1.Hkv)
+            secs, flops, reps = secs + s1, flops + f1, reps + 1
+    finally:
+        oracle.set_threads(0)
+    return {"workload": w1.name, "value": round(flops / secs / 1e12, 6), "unit": "TFLOPS", "cores": 1,
+            "ms_per_step": round(1e3 * secs / reps, 3), "sample": f"{reps} fwd+bwd passes of the whole workload"}
+
+
 def _cpu_baseline(w, host, budget_s: float):
     threads = os.cpu_count() or 1
     secs, flops = _cpu_sample(w, host, 1)
@@ -608,7 +700,8 @@ def _cpu_baseline(w, host, budget_s: float):
             secs, flops, n = secs + s2, flops + f2, 1 + min(extra, w.B * w.Hkv)
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
             "sample": f"fp64 oracle forward+backward of {n} (batch, kv-head) group(s) of {w.name} at full "
-                      f"N={w.N}, {secs:.1f} s, OpenMP over {threads} host threads"}
+                      f"N={w.N}, {secs:.1f} s, OpenMP over {threads} host threads",
+            "single_thread": _cpu_single_thread_small()}
 
 
 def run_reference(a):

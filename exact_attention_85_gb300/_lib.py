@@ -21,7 +21,7 @@ EXPORTS = (
     "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_two_pass", "fa_bwd_two_pass_workspace_bytes",
     "fa_bwd_noalloc", "fa_hadamard_quant_fp8",
     "fa_hadamard_quant_workspace_bytes", "fa_fwd_fp8", "fa_get_device_status",
-    "fa_selftest_bounded_wait", "fa_status_string",
+    "fa_selftest_bounded_wait", "fa_status_string", "fa_fwd_f32_out", "fa_probe_exp2",
 )
 
 _lock = threading.Lock()
@@ -47,6 +47,7 @@ def load():
         P, I, F, Z, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_long
         lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_fwd_local.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
+        lib.fa_fwd_f32_out.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_bwd_local.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, Z, P]
         lib.fa_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P]
         lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, Z, P]
@@ -65,6 +66,8 @@ def load():
         lib.fa_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.fa_get_device_status.argtypes = [P]
         lib.fa_selftest_bounded_wait.argtypes = [I, P]
+        lib.fa_probe_exp2.argtypes = [P, I, I, P]
+        lib.fa_probe_exp2.restype = ctypes.c_longlong
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         for name in ("fa_fwd", "fa_fwd_local", "fa_bwd_local", "fa_fwd_varlen", "fa_bwd_varlen", "fa_bwd", "fa_bwd_two_pass", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
@@ -111,6 +114,14 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None):
     B, Hq, Hkv, N, d = _dims(q, k)
     _check("fa_fwd", load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
                                    int(causal), float(scale), _dtype_code(q), _stream(stream)))
+
+
+def fa_fwd_f32_out(q, k, v, o_f32, lse, causal: bool, scale: float, stream=None):
+    """fa_fwd with O written in fp32 (o_f32 [B,Hq,N,d] float32): the
+    normalised accumulator before rounding to the input type."""
+    B, Hq, Hkv, N, d = _dims(q, k)
+    _check("fa_fwd_f32_out", load().fa_fwd_f32_out(_ptr(q), _ptr(k), _ptr(v), _ptr(o_f32), _ptr(lse), B, Hq, Hkv,
+                                                   N, d, int(causal), float(scale), _dtype_code(q), _stream(stream)))
 
 
 def fa_fwd_local(q, k, v, o, lse, window: int, scale: float, stream=None):
@@ -221,3 +232,14 @@ def fa_get_device_status(stream=None) -> int:
 
 def fa_selftest_bounded_wait(timeout_us: int, stream=None):
     _check("fa_selftest_bounded_wait", load().fa_selftest_bounded_wait(int(timeout_us), _stream(stream)))
+
+
+def fa_probe_exp2(sink, blocks: int, iters: int, stream=None) -> int:
+    """Launches the exp2 throughput probe; returns the exp2 evaluations it
+    performs.  sink: float32 CUDA tensor of at least blocks * 256 elements."""
+    if sink.numel() < blocks * 256:
+        raise ValueError("sink too small")
+    n = load().fa_probe_exp2(_ptr(sink), int(blocks), int(iters), _stream(stream))
+    if n < 0:
+        raise FAError("fa_probe_exp2", FA_ERR_INVALID_ARG, "invalid arguments or launch failure")
+    return int(n)

@@ -132,7 +132,7 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 // Shared validation and launch of the forward entry points (window 0: none).
 fa_status_t fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
                        int N, int d, int causal, int window, float scale, fa_dtype_t dtype, void *stream,
-                       const fa::SeqLayout *packed = nullptr) {
+                       const fa::SeqLayout *packed = nullptr, bool o_f32 = false) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
@@ -141,7 +141,7 @@ fa_status_t fwd_common(const void *q, const void *k, const void *v, void *o, flo
     if (s != FA_OK) return s;
     fa::SeqLayout lay{0, B, N, B * N, nullptr};
     if (packed) lay = *packed;
-    fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, dtype == FA_BF16, window, lay};
+    fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, dtype == FA_BF16, window, lay, o_f32};
     return from_cuda(fa::launch_fwd(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -193,6 +193,12 @@ const char *fa_status_string(fa_status_t s) {
 fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
                    int N, int d, int causal, float scale, fa_dtype_t dtype, void *stream) {
     return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, stream);
+}
+
+fa_status_t fa_fwd_f32_out(const void *q, const void *k, const void *v, float *o_f32, float *lse, int B, int Hq,
+                           int Hkv, int N, int d, int causal, float scale, fa_dtype_t dtype, void *stream) {
+    return fwd_common(q, k, v, o_f32, lse, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, stream, nullptr,
+                      true);
 }
 
 fa_status_t fa_fwd_local(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
@@ -320,6 +326,14 @@ fa_status_t fa_get_device_status(void *stream) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
     if (host & fa::kStatusTimeout) return FA_ERR_TIMEOUT;
     return (host & fa::kStatusBadArgs) ? FA_ERR_INVALID_ARG : FA_OK;
+}
+
+long long fa_probe_exp2(float *sink, int blocks, int iters, void *stream) {
+    if (!sink || !aligned16(sink) || blocks < 1 || blocks > 65535 || iters < 1 || iters > (1 << 24)) return -1;
+    long long exps = 0;
+    if (fa::launch_ex2_rate(sink, blocks, iters, &exps, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return -1;
+    return exps;
 }
 
 fa_status_t fa_selftest_bounded_wait(int timeout_us, void *stream) {

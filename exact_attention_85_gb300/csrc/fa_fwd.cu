@@ -76,6 +76,7 @@ struct FwdParams {
     int Hq, Hkv, N, nblk, causal;  // N: rows per sequence (packed: the maximum); nblk: 256-row blocks
     int group, planes;             // CTA order (grid_order.cuh): planes per group, B * Hq
     int window;                    // > 0: row r sees keys r - window + 1 .. r only
+    int o_f32;                     // O is written in fp32 (before any rounding to the 16-bit type)
     float scale_log2;              // scale * log2(e)
 };
 
@@ -108,6 +109,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int win = GENERAL ? p.window : 0;
     const bool packed = GENERAL && p.varlen;
+    const bool o_f32 = GENERAL && p.o_f32;
+    const bool rows_out = packed || o_f32;  // each thread stores its own output row
 
     // CTA order: planes in L2-sized groups, longest causal blocks first
     int bh, t_lin;
@@ -462,23 +465,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t o[32];
                     tmem_ld_x32(lane_base + col_o + c0, o);
                     tmem_ld_wait_x32(o);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * inv_l);
                     uint32_t w[16];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float a = __uint_as_float(o[2 * c]) * inv_l;
-                        const float bb = __uint_as_float(o[2 * c + 1]) * inv_l;
-                        w[c] = BF16 ? pack_bf16x2(a, bb) : pack_f16x2(a, bb);
-                    }
-                    if (packed) {
+                    for (int c = 0; c < 16; ++c)
+                        w[c] = BF16 ? pack_bf16x2(__uint_as_float(o[2 * c]), __uint_as_float(o[2 * c + 1]))
+                                    : pack_f16x2(__uint_as_float(o[2 * c]), __uint_as_float(o[2 * c + 1]));
+                    if (rows_out) {
                         // packed rows: a 128-row box past this sequence's end
-                        // would overwrite the next sequence, so each thread
-                        // stores its own row (16-byte stores)
+                        // would overwrite the next sequence; fp32 rows: the box
+                        // is laid out for 16-bit elements.  So each thread
+                        // stores its own row (16-byte stores).
                         if (q0 + row < N) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.o) +
-                                                                   ((size_t)(row0 + q0 + row) * p.Hq + h) * (D * 2));
+                            const size_t r = packed ? (size_t)(row0 + q0 + row) * p.Hq + h
+                                                    : (size_t)q_plane * N + q0 + row;
+                            if (o_f32) {
+                                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<float *>(p.o) + r * D + c0);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                dst[c0 / 8 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                                for (int q = 0; q < 8; ++q)
+                                    dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                            } else {
+                                uint4 *dst =
+                                    reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.o) + r * (D * 2)) + c0 / 8;
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                            }
                         }
                     } else {
                         uint8_t *rowp = stage + (c0 >> 6) * L::BOX + row * 128;
@@ -490,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (!packed) {
+                if (!rows_out) {
                     fence_proxy_async_smem();
                     named_bar_sync(1 + x, kBM);
                     if (row == 0) {
@@ -525,7 +538,7 @@ cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t st) {
     if (!make_tmap_tiles(&tq, a.q, dt, D, a.lay, a.Hq, kBM) || !make_tmap_tiles(&tk, a.k, dt, D, a.lay, a.Hkv, kBN) ||
         !make_tmap_tiles(&tv, a.v, dt, D, a.lay, a.Hkv, kBN) || !make_tmap_tiles(&to, a.o, dt, D, a.lay, a.Hq, kBM))
         return cudaErrorInvalidValue;
-    const bool general = a.window > 0 || a.lay.varlen;
+    const bool general = a.window > 0 || a.lay.varlen || a.o_f32;
     auto kernel = general ? fwd_kernel<D, BF16, true> : fwd_kernel<D, BF16, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
@@ -549,6 +562,7 @@ cudaError_t launch_fwd_t(const FwdArgs &a, cudaStream_t st) {
     }
     p.causal = a.causal;
     p.window = a.window;
+    p.o_f32 = a.o_f32 ? 1 : 0;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     const long long grid = (long long)p.nblk * a.B * a.Hq;
     kernel<<<dim3((unsigned)grid), dim3(kThreads), L::ALLOC, st>>>(tq, tk, tv, to, p);

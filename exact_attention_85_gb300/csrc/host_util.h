@@ -52,6 +52,7 @@ struct FwdArgs {
     bool bf16;
     int window;  // 0: none; > 0: causal sliding window of that many keys
     SeqLayout lay;
+    bool o_f32;  // O written as fp32 (debug output), else in the input type
 };
 
 struct BwdArgs {
@@ -91,5 +92,6 @@ cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool two_pass);
 cudaError_t launch_fwd_fp8(const Fp8FwdArgs &a, cudaStream_t st);
 cudaError_t launch_hadamard_quant(const QuantArgs &a, cudaStream_t st);
 cudaError_t launch_selftest_wait(int timeout_us, cudaStream_t st);
+cudaError_t launch_ex2_rate(float *sink, int blocks, int iters, long long *exps, cudaStream_t st);
 
 }  // namespace fa

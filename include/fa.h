@@ -67,6 +67,22 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
                    int causal, float scale, fa_dtype_t dtype, void *stream);
 
 /*
+ * Debug forward: fa_fwd with O written in fp32, i.e. O~ / l before any
+ * rounding to the 16-bit type, so that the kernel's own arithmetic can be
+ * checked without the output's rounding.  [V2] section 6.1 (the final
+ * diag(l)^-1 rescale of O~).  Same kernel and schedule; each thread stores
+ * its output row directly instead of staging a 16-bit tile for TMA.
+ *   Arguments, layouts and errors as fa_fwd, except
+ *   o_f32 [B][Hq][N][d] fp32 (out, 16-byte aligned).
+ * O still carries the rounding of P to the 16-bit type that the P.V tensor
+ * core product consumes.
+ */
+fa_status_t fa_fwd_f32_out(const void *q, const void *k, const void *v,
+                           float *o_f32, float *lse, int B, int Hq, int Hkv,
+                           int N, int d, int causal, float scale,
+                           fa_dtype_t dtype, void *stream);
+
+/*
  * Causal sliding-window ("local") forward: fa_fwd with causal = 1 and the
  * additional mask that query row r sees only the `window` most recent keys,
  * r - window + 1 .. r (its own key included).
@@ -285,6 +301,21 @@ fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8,
  * FA_ERR_TIMEOUT (or FA_ERR_CUDA if the copy itself fails).
  */
 fa_status_t fa_get_device_status(void *stream);
+
+/*
+ * Measurement aid: launches `blocks` blocks of 256 threads, each thread
+ * running `iters` rounds of eight independent exp2 evaluations with the
+ * instruction the softmax uses, and returns how many exp2 evaluations the
+ * launch performs (or -1 for invalid arguments or a failed launch).  Timing
+ * the launch on `stream` gives the exp2 throughput that bounds the softmax
+ * ([FA3] "overlapping GEMM and softmax": the exponential runs on a separate
+ * unit far slower than the tensor cores).
+ *   sink [blocks * 256] fp32 (out, device, 16-byte aligned): per thread the
+ *        sum of its eight chains, in [-8, -6.3], written so that the work
+ *        is not removed
+ *   blocks 1 .. 65535, iters 1 .. 2^24
+ */
+long long fa_probe_exp2(float *sink, int blocks, int iters, void *stream);
 
 /*
  * Self-test of the bounded-wait machinery: launches one block that waits on a

@@ -72,11 +72,22 @@ def _load():
             lib.oracle_bwd.argtypes = [P, P, P, P, P, P, P, L, L, L, L, L, ctypes.c_int, L, ctypes.c_double]
             lib.oracle_hadamard.argtypes = [P, P, P, L, L]
             lib.oracle_e4m3_round.argtypes = [P, P, L]
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
+            lib.oracle_set_threads.restype = None
+            lib.oracle_get_threads.restype = ctypes.c_int
             for name in ("oracle_fwd", "oracle_fwd_rows", "oracle_bwd_group",
                          "oracle_bwd", "oracle_hadamard", "oracle_e4m3_round"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
+
+
+def set_threads(n: int) -> int:
+    """Threads the oracle's loops use from now on (n < 1: all host
+    processors); returns the count in effect.  Results do not depend on it."""
+    lib = _load()
+    lib.oracle_set_threads(int(n))
+    return int(lib.oracle_get_threads())
 
 
 def _f64(x) -> np.ndarray:

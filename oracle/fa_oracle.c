@@ -40,8 +40,14 @@
  * e4m3 ("fn") grid with saturation at +-448.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Threads of the OpenMP loops below, for timing baselines (n < 1: one per
+ * host processor, the default).  No effect on any result. */
+void oracle_set_threads(int n) { omp_set_num_threads(n >= 1 ? n : omp_get_num_procs()); }
+int oracle_get_threads(void) { return omp_get_max_threads(); }
 
 #define IDX4(b, h, n, H, N) ((((long)(b) * (H) + (h)) * (N) + (n)))
 

@@ -56,3 +56,30 @@ def check_grad(got, ref: np.ndarray, what: str):
     r = rel_fro(got, ref)
     assert r <= GRAD_REL, f"{what}: relative Frobenius error {r:.3e} > {GRAD_REL}"
     return r
+
+
+def p_rounding_bound(q, k, v, causal: bool, scale: float, o_ref: np.ndarray, p_dtype) -> np.ndarray:
+    """Element-wise bound on |O~/l - O| that rounding P to `p_dtype` alone
+    can cause, when l sums the same rounded P (the forward's P.V operand).
+
+    With P^_c = P_c (1 + e_c), |e_c| <= u (round to nearest, u = 2^-(mant+1)):
+    O^ - O = sum_c P_c e_c (V_c - O) / sum_c P^_c, so
+    |O^ - O| <= u / (1 - u) * sum_c Pbar_c |V_c - O| with Pbar = P / sum P.
+    Plain fp64 softmax of the small test shapes (no tiling)."""
+    u = 2.0 ** -(_MANT[p_dtype] + 1)
+    Q, K, V = (np.asarray(t.double().numpy() if hasattr(t, "numpy") else t, dtype=np.float64) for t in (q, k, v))
+    B, Hq, N, d = Q.shape
+    G = Hq // K.shape[1]
+    out = np.empty_like(o_ref)
+    for b in range(B):
+        for h in range(Hq):
+            s = scale * Q[b, h] @ K[b, h // G].T
+            if causal:
+                s[np.triu_indices(N, 1)] = -np.inf
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            Vh = V[b, h // G]
+            # sum_c p[r, c] |V[c, j] - O[r, j]|, row by row to bound memory
+            for r in range(N):
+                out[b, h, r] = p[r] @ np.abs(Vh - o_ref[b, h, r][None, :])
+    return u / (1.0 - u) * out

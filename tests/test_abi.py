@@ -90,6 +90,18 @@ def test_fp8_argument_validation(lib):
     assert lib.fa_selftest_bounded_wait(2000000, None) == 1
 
 
+def test_debug_and_probe_argument_validation(lib):
+    lib.fa_probe_exp2.restype = ctypes.c_longlong
+    assert lib.fa_probe_exp2(None, 1, 1, None) == -1
+    assert lib.fa_probe_exp2(FAKE + 4, 1, 1, None) == -1
+    assert lib.fa_probe_exp2(FAKE, 0, 1, None) == -1
+    assert lib.fa_probe_exp2(FAKE, 1, 0, None) == -1
+    assert lib.fa_probe_exp2(FAKE, 70000, 1, None) == -1
+    args = [FAKE] * 5 + [1, 2, 1, 16, 128, 0, 0.1, 1, None]
+    assert lib.fa_fwd_f32_out(*([None] + args[1:])) == 1
+    assert lib.fa_fwd_f32_out(*(args[:9] + [96] + args[10:])) == 2
+
+
 def test_product_path_does_not_reference_oracle():
     """The CUDA library and its binding never import, link or call the oracle."""
     pkg = os.path.join(ROOT, "exact_attention_85_gb300")

@@ -114,3 +114,47 @@ def test_bounded_wait_selftest(cuda_lib):
     x = make_custom(1, 1, 1, 64, 64, torch.bfloat16, seed=1, with_grad=False)
     o, _ = _run_fwd(x, False, 0.125)
     assert torch.isfinite(o).all()
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,dtype,causal", [
+    (1, 2, 1, 700, 128, torch.bfloat16, True),
+    (1, 2, 2, 300, 64, torch.float16, True),
+    (2, 2, 1, 257, 128, torch.float16, False),
+])
+def test_fwd_f32_out_meets_rounding_bound(cuda_lib, B, Hq, Hkv, N, d, dtype, causal):
+    """Debug output: O~ / l in fp32, before rounding to the 16-bit type.  What
+    is left is the rounding of P itself (the P.V operand): each element lies
+    within the bound that rounding alone allows (tests/_tol.p_rounding_bound)
+    plus 1e-4 for fp32 accumulation; fp16 (u = 2^-11) meets the raw 4e-3
+    bound everywhere, and both meet it on rows >= 128."""
+    from _tol import p_rounding_bound
+    x = make_custom(B, Hq, Hkv, N, d, dtype, seed=N + 17 * d, with_grad=False)
+    scale = d ** -0.5
+    q, k, v = (x[n].cuda().contiguous() for n in ("q", "k", "v"))
+    o32 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+    _lib.fa_fwd_f32_out(q, k, v, o32, lse, causal, scale)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    o_ref, lse_ref = oracle.attention_fwd(x["q"], x["k"], x["v"], causal, scale)
+    err = np.abs(o32.cpu().numpy().astype(np.float64) - o_ref)
+    bound = p_rounding_bound(x["q"], x["k"], x["v"], causal, scale, o_ref, dtype) + 1e-4
+    assert (err <= bound).all(), f"max excess {(err - bound).max():.3e}"
+    assert err[:, :, 128:].max() <= 4e-3
+    if dtype == torch.float16:
+        assert err.max() <= 4e-3
+    check_lse(lse, lse_ref)
+    # same kernel, 16-bit output: the stored O is the fp32 value rounded
+    o16 = torch.empty_like(q)
+    _lib.fa_fwd(q, k, v, o16, lse, causal, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o16, o32.to(dtype))
+
+
+def test_exp2_probe(cuda_lib):
+    sink = torch.empty(4 * 256, dtype=torch.float32, device="cuda")
+    n = _lib.fa_probe_exp2(sink, 4, 3)
+    torch.cuda.synchronize()
+    assert n == 4 * 256 * 8 * 3
+    s = sink.cpu()
+    assert torch.isfinite(s).all() and (s >= -8.0).all() and (s <= -6.3).all()

@@ -473,3 +473,24 @@ def test_varlen_matches_block_diagonal_sdpa(causal, window):
     for h in range(Hq):
         s = np.where(mask, scale * q[:, h] @ k[:, h // G].T, -np.inf)
         np.testing.assert_allclose(lse[h], logsumexp(s, axis=1), atol=1e-12)
+
+
+def test_thread_count_does_not_change_results():
+    """The OpenMP thread count (set for the single-thread timing baseline)
+    leaves every result bit-identical: each output element is computed by
+    one thread in a fixed order."""
+    g = torch.Generator().manual_seed(3)
+    q, k, v, dO = (torch.randn(1, 4, 97, 64, generator=g, dtype=torch.float64) for _ in range(4))
+    k, v = k[:, :2], v[:, :2]
+    try:
+        oracle.set_threads(1)
+        o1, l1 = oracle.attention_fwd(q, k, v, True, 0.125)
+        g1 = oracle.attention_bwd(q, k, v, dO, True, 0.125)
+        assert oracle.set_threads(3) == 3
+        o3, l3 = oracle.attention_fwd(q, k, v, True, 0.125)
+        g3 = oracle.attention_bwd(q, k, v, dO, True, 0.125)
+    finally:
+        oracle.set_threads(0)
+    assert np.array_equal(o1, o3) and np.array_equal(l1, l3)
+    for a, b in zip(g1, g3):
+        assert np.array_equal(a, b)
