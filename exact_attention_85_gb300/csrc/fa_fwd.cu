@@ -266,27 +266,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if constexpr (!GENERAL) {
                 // full causal or no mask: both tiles start at K/V tile 0
-                for (int j = 0; ok && j < nmax; ++j) {
-                    if (!mbar_wait(&v_full[j % L::VS], (j / L::VS) & 1, abort_flag, p.status, 6)) {
-                        ok = false;
-                        break;
-                    }
+                if (ok && nmax > 0) {
+                    ok = mbar_wait(&v_full[0], 0, abort_flag, p.status, 6);
                     tc_fence_after();
-                    for (int x = 0; x < 2; ++x) {
-                        const int nx = x ? nB : nA;
-                        if (j >= nx) continue;
-                        if (!issue_pv(x, j, j)) { ok = false; break; }
-                        if (j + 1 < nx) {
-                            // S_x(j+1) overwrites P_x(j), which the MMAs just issued read first
-                            if (!wait_k(j + 1)) { ok = false; break; }
-                            issue_s(x, j + 1);
-                        } else {
-                            mma_commit(&o_final[x]);
-                        }
+                }
+                // K_j's slot is released after the first P.V of tile j (one
+                // step later than its last reader, S_B(j), needs), and V_{j+1}
+                // is checked before S_B(j+1): the issuing thread then goes from
+                // the last S MMA of one step straight to the first P.V of the next
+                for (int j = 0; ok && j < nmax; ++j) {
+                    // V_j is ready here
+                    if (j < nA) {
+                        if (!issue_pv(0, j, j)) { ok = false; break; }
                     }
-                    if (!ok) break;
+                    if (j >= 1) mma_commit(&k_empty[j % L::KS]);  // K_j: last read by S_B(j)
+                    if (j + 1 < nA) {
+                        if (!wait_k(j + 1)) { ok = false; break; }
+                        issue_s(0, j + 1);
+                    } else if (j < nA) {
+                        mma_commit(&o_final[0]);
+                    }
+                    if (j < nB) {
+                        if (!issue_pv(1, j, j)) { ok = false; break; }
+                    }
                     mma_commit(&v_empty[j % L::VS]);
-                    if (j + 1 < nmax) mma_commit(&k_empty[(j + 1) % L::KS]);
+                    if (j + 1 < nmax) {
+                        if (!mbar_wait(&v_full[(j + 1) % L::VS], ((j + 1) / L::VS) & 1, abort_flag, p.status, 6)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    if (j + 1 < nB) {
+                        if (!wait_k(j + 1)) { ok = false; break; }
+                        issue_s(1, j + 1);
+                    } else if (j < nB) {
+                        mma_commit(&o_final[1]);
+                    }
                 }
             } else {
                 for (int j = jA0; ok && j < nmax; ++j) {
