@@ -271,15 +271,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kStage = 2 * L::TILE_Q;  // bytes between Q/dO stages
             bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 22);
 
-            // S^T = K_j Q_t^T -> [0, 128) (commit s_full), then dP^T = V_j dO_t^T
+            // S^T = K_j Q_t^T -> [0, 128) (commit s_full), and dP^T = V_j dO_t^T
             // -> [128, 256) (commit dp_full): the softmax warps start on P^T as
             // soon as S^T is there, while the tensor cores compute dP^T
-            auto issue_sdp = [&](int t) -> bool {
+            auto issue_s = [&](int t) -> bool {
                 const int st = t % QS;
                 if (!mbar_wait(&qd_full[st], (t / QS) & 1, abort_flag, p.status, 23)) return false;
                 tc_fence_after();
                 const uint64_t q_desc = sdesc_advance(qk_desc0, st * kStage);
-                const uint64_t do_desc = sdesc_advance(dok_desc0, st * kStage);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
@@ -288,6 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                kk > 0 ? 1u : 0u);
                 }
                 mma_commit(s_full);
+                return true;
+            };
+            auto issue_dp = [&](int t) {
+                const uint64_t do_desc = sdesc_advance(dok_desc0, (t % QS) * kStage);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t okv = (kk >> 2) * L::BOX_KV + (kk & 3) * 32;
@@ -296,10 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                kk > 0 ? 1u : 0u);
                 }
                 mma_commit(dp_full);
-                return true;
             };
 
-            if (ok) ok = issue_sdp(0);
+            if (ok) ok = issue_s(0);
+            if (ok) issue_dp(0);
             for (int it = 0; ok && it < n_it; ++it) {
                 const int st = it % QS;
                 const uint64_t qm_desc = sdesc_advance(qm_desc0, st * kStage);
@@ -317,6 +320,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                kk > 0 ? 1u : acc_first);
                 if (!mbar_wait(ds_ready, it & 1, abort_flag, p.status, 24)) { ok = false; break; }
                 tc_fence_after();
+                // dK_j += dS^T Q_i (A from tensor memory, as for dV); it is the
+                // last reader of this Q/dO stage
+#pragma unroll
+                for (int kk = 0; kk < kBQ / 16; ++kk)
+                    mma_f16_ts(tmem + kColDK, tmem + kColS + kk * 16 + 8, sdesc_advance(qm_desc, kk * 2048),
+                               idesc_acc, kk > 0 ? 1u : acc_first);
+                mma_commit(&qd_empty[st]);
+                // S^T of the next tile overwrites P^T, dS^T (read by the MMAs just
+                // issued, which run first): issued before dQ^T so that the
+                // softmax warps start on the next tile one GEMM earlier
+                if (it + 1 < n_it && !issue_s(it + 1)) { ok = false; break; }
                 // dQ_i^T = K_j^T dS_i^T -> [128, 256) (lane = head-dim index);
                 // 16 keys = 16 rows = 2048 bytes of both operands per step
                 if constexpr (DQ) {
@@ -326,20 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    sdesc_advance(ds_desc, kk * 2048), idesc_dq, kk > 0 ? 1u : 0u);
                     mma_commit(dq_full);
                 }
-                // dK_j += dS^T Q_i (A from tensor memory, as for dV)
-#pragma unroll
-                for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDK, tmem + kColS + kk * 16 + 8, sdesc_advance(qm_desc, kk * 2048),
-                               idesc_acc, kk > 0 ? 1u : acc_first);
-                mma_commit(&qd_empty[st]);
                 if (it + 1 < n_it) {
-                    // S^T / dP^T of the next tile overwrite P^T, dS^T (read by the MMAs
-                    // just issued, which run first) and dQ^T (read out once dq_free flips)
+                    // dP^T of the next tile overwrites dQ^T, read out once dq_free flips
                     if constexpr (DQ) {
                         if (!mbar_wait(dq_free, it & 1, abort_flag, p.status, 25)) { ok = false; break; }
+                        tc_fence_after();
                     }
-                    tc_fence_after();
-                    if (!issue_sdp(it + 1)) { ok = false; break; }
+                    issue_dp(it + 1);
                 }
             }
             if (ok) mma_commit(acc_done);
