@@ -31,10 +31,11 @@
 // dK += dS^T Q; dS^T is also written to shared memory as the B operand of
 // dQ^T = K^T dS^T.  Per Q tile: MMA S^T -> softmax phase 1 (P^T) while the
 // tensor cores compute dP^T -> MMA dV += P^T dO while softmax phase 2 forms
-// dS^T -> MMA dQ^T, dK -> read-out warps copy dQ^T out of tensor memory
-// (which frees the columns for the next S^T, dP^T) and add it into dQacc
-// with fp32 atomic reductions (one 128-byte line per warp and query row)
-// while the softmax warps already work on the next tile.
+// dS^T -> MMA dK, then the next tile's S^T (the softmax warps start on it
+// while the tensor cores go on), then dQ^T -> read-out warps copy dQ^T out of
+// tensor memory (which frees the columns for the next dP^T) and add it into
+// dQacc with fp32 atomic reductions (one 128-byte line per warp and query
+// row) while the softmax warps work on the next tile.
 // Warps: 0-7 softmax (then 0-3 store dV, 4-7 store dK), 8-15 dQ read-out
 // (softmax too when the kernel runs without its dQ part), 16 TMA producer
 // (Q / dO through a 2-deep ring), 17 MMA issuer + TMEM owner.
