@@ -70,8 +70,8 @@ struct BwdLayout {
     static constexpr int OFF_LD = OFF_DS + DS_BYTES;  // stage s: L2[128], D[128]
     static constexpr int OFF_BAR = OFF_LD + QS * 2 * kBQ * 4;
     // kv_full, qd_full[QS], qd_empty[QS], s_full, dp_full, p_ready, ds_ready,
-    // dq_full, dq_free, acc_done, drain
-    static constexpr int NBAR = 1 + 2 * QS + 6 + 2;
+    // dq_full, dq_free, acc_done, drain, ds_half
+    static constexpr int NBAR = 1 + 2 * QS + 6 + 3;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SLACK = 512;  // room to align the dynamic shared base up to 1024
@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *dq_free = dq_full + 1;
     uint64_t *acc_done = dq_free + 1;
     uint64_t *drain = acc_done + 1;
+    uint64_t *ds_half = drain + 1;  // dS^T of every warp's first half of query chunks is in TMEM
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
     float *ld_smem = reinterpret_cast<float *>(smem + L::OFF_LD);
@@ -180,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(dp_full, 1);
         mbar_init(p_ready, kSmWarps * 32);
         mbar_init(ds_ready, kSmWarps * 32);
+        mbar_init(ds_half, kSmWarps * 32);
         mbar_init(dq_full, 1);
         mbar_init(dq_free, kReadoutThreads);
         mbar_init(acc_done, 1);
@@ -319,15 +321,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < kBQ / 16; ++kk)
                     mma_f16_ts(tmem + kColDV, tmem + kColS + kk * 16, sdesc_advance(dom_desc, kk * 2048), idesc_acc,
                                kk > 0 ? 1u : acc_first);
+                // dK_j += dS^T Q_i (A from tensor memory, as for dV), as two sets
+                // of 16-query steps: those with (step mod 4) < 2 -- with dQ,
+                // the first two chunks of every softmax warp, issued as soon
+                // as they are written (ds_half) so that they run during the
+                // rest of the second phase -- then the others.  Without dQ the
+                // same order is kept (one wait), so that both variants sum dK
+                // identically.
+                auto issue_dk = [&](bool first) {
+#pragma unroll
+                    for (int kk = 0; kk < kBQ / 16; ++kk)
+                        if (((kk & 3) < 2) == first)
+                            mma_f16_ts(tmem + kColDK, tmem + kColS + kk * 16 + 8, sdesc_advance(qm_desc, kk * 2048),
+                                       idesc_acc, kk > 0 ? 1u : acc_first);
+                };
+                if constexpr (DQ) {
+                    if (!mbar_wait(ds_half, it & 1, abort_flag, p.status, 32)) { ok = false; break; }
+                    tc_fence_after();
+                    issue_dk(true);
+                }
                 if (!mbar_wait(ds_ready, it & 1, abort_flag, p.status, 24)) { ok = false; break; }
                 tc_fence_after();
-                // dK_j += dS^T Q_i (A from tensor memory, as for dV); it is the
-                // last reader of this Q/dO stage
-#pragma unroll
-                for (int kk = 0; kk < kBQ / 16; ++kk)
-                    mma_f16_ts(tmem + kColDK, tmem + kColS + kk * 16 + 8, sdesc_advance(qm_desc, kk * 2048),
-                               idesc_acc, kk > 0 ? 1u : acc_first);
-                mma_commit(&qd_empty[st]);
+                if constexpr (!DQ) issue_dk(true);
+                issue_dk(false);
+                mma_commit(&qd_empty[st]);  // dK is the last reader of this Q/dO stage
                 // S^T of the next tile overwrites P^T, dS^T (read by the MMAs just
                 // issued, which run first): issued before dQ^T so that the
                 // softmax warps start on the next tile one GEMM earlier
@@ -472,6 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 // dS^T into the last 8 of the chunk's 16 S^T columns
                 tmem_st_x8(lane_base + kColS + qc + 8, dd);
+                if (DQ && ch == kNCH / 2 - 1) {
+                    // the first half of this warp's chunks is in tensor memory:
+                    // the dK MMAs for those queries may start
+                    tmem_st_wait();
+                    tc_fence_before();
+                    mbar_arrive(ds_half);
+                }
                 if constexpr (DQ) {
                     // dS^T row c, queries qc .. qc + 15 -> 16-byte chunks 2 ch, 2 ch + 1
                     // of the 128-byte swizzled row of box hf
