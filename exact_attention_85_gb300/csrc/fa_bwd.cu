@@ -70,8 +70,8 @@ struct BwdLayout {
     static constexpr int OFF_LD = OFF_DS + DS_BYTES;  // stage s: L2[128], D[128]
     static constexpr int OFF_BAR = OFF_LD + QS * 2 * kBQ * 4;
     // kv_full, qd_full[QS], qd_empty[QS], s_full, dp_full, p_ready, ds_ready,
-    // dq_full, dq_free, acc_done, drain, ds_half
-    static constexpr int NBAR = 1 + 2 * QS + 6 + 3;
+    // dq_full, dq_free, acc_done, drain, ds_half, ds_smem
+    static constexpr int NBAR = 1 + 2 * QS + 6 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SLACK = 512;  // room to align the dynamic shared base up to 1024
@@ -127,7 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *dq_free = dq_full + 1;
     uint64_t *acc_done = dq_free + 1;
     uint64_t *drain = acc_done + 1;
-    uint64_t *ds_half = drain + 1;  // dS^T of every warp's first half of query chunks is in TMEM
+    uint64_t *ds_half = drain + 1;
+    uint64_t *ds_smem = ds_half + 1;  // dS^T is in shared memory (the B operand of dQ^T)  // dS^T of every warp's first half of query chunks is in TMEM
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
     float *ld_smem = reinterpret_cast<float *>(smem + L::OFF_LD);
@@ -182,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(p_ready, kSmWarps * 32);
         mbar_init(ds_ready, kSmWarps * 32);
         mbar_init(ds_half, kSmWarps * 32);
+        mbar_init(ds_smem, kSmWarps * 32);
         mbar_init(dq_full, 1);
         mbar_init(dq_free, kReadoutThreads);
         mbar_init(acc_done, 1);
@@ -352,6 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // dQ_i^T = K_j^T dS_i^T -> [128, 256) (lane = head-dim index);
                 // 16 keys = 16 rows = 2048 bytes of both operands per step
                 if constexpr (DQ) {
+                    if (!mbar_wait(ds_smem, it & 1, abort_flag, p.status, 33)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kBKV / 16; ++kk)
                         mma_f16_ss(tmem + kColDQ, sdesc_advance(kt_desc, kk * 2048),
@@ -460,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
             uint32_t dpv[32];  // dP^T of two chunks at a time
+            uint32_t ddk[kNCH][8];  // packed dS^T, kept for the shared-memory copy
 #pragma unroll
             for (int ch = 0; ch < kNCH; ++ch) {
                 const int qc = q0w + ch * 16;
@@ -496,19 +501,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     mbar_arrive(ds_half);
                 }
-                if constexpr (DQ) {
-                    // dS^T row c, queries qc .. qc + 15 -> 16-byte chunks 2 ch, 2 ch + 1
-                    // of the 128-byte swizzled row of box hf
 #pragma unroll
-                    for (int q = 0; q < 2; ++q)
-                        *reinterpret_cast<uint4 *>(ds_row + (((2 * ch + q) ^ (c & 7)) << 4)) =
-                            make_uint4(dd[4 * q], dd[4 * q + 1], dd[4 * q + 2], dd[4 * q + 3]);
-                }
+                for (int r = 0; r < 8; ++r) ddk[ch][r] = dd[r];
             }
-            if constexpr (DQ) fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(ds_ready);
+            if constexpr (DQ) {
+                // the shared-memory copy for dQ^T after ds_ready, so that dK and
+                // the next S^T do not wait for these stores; dQ^T waits on ds_smem
+#pragma unroll
+                for (int ch = 0; ch < kNCH; ++ch)
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        *reinterpret_cast<uint4 *>(ds_row + (((2 * ch + q) ^ (c & 7)) << 4)) =
+                            make_uint4(ddk[ch][4 * q], ddk[ch][4 * q + 1], ddk[ch][4 * q + 2], ddk[ch][4 * q + 3]);
+                fence_proxy_async_smem();
+                mbar_arrive(ds_smem);
+            }
         }
         // ------------------------------- epilogue: dV (warps 0-3), dK (warps 4-7)
         bool ok2 = ok && warp < 8 && mbar_wait(acc_done, 0, abort_flag, p.status, 28);
