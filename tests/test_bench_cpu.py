@@ -1,0 +1,43 @@
+"""Host-side checks of the benchmark script: the reference arm's JSON line
+(it times the fp64 oracle, so it runs without a GPU) and the FLOP / exp
+counting helpers the GPU legs use."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOPS" and d["higher_is_better"] is True
+    assert d["steps"] == 1 and d["warmup"] == 0 and d["n_gpus"] == 1 and d["dtype"] == "f64"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"]["workload"] == "bf16_b4_h16_n8k_d128_causal"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_visible_pairs_and_flop_counts():
+    import bench
+    from exact_attention_85_gb300.inputs import WORKLOADS
+
+    w = WORKLOADS["bf16_b4_h16_n8k_d128_causal"]
+    # causal: row r sees r + 1 keys, so N (N + 1) / 2 pairs per head
+    assert bench._visible_pairs(w) == 4 * 16 * 8192 * 8193 / 2
+    # the metric's convention: 4 B H N^2 d, halved for causal; backward 2.5x
+    assert w.fwd_flops() == pytest.approx(4 * 4 * 16 * 8192 ** 2 * 128 / 2)
+    assert w.bwd_flops() == pytest.approx(2.5 * w.fwd_flops())
+    t = WORKLOADS["tiny_fp16_d64_n256"]
+    assert not t.causal and bench._visible_pairs(t) == t.B * t.Hq * 256 * 256
