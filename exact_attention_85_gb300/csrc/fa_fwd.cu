@@ -431,8 +431,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[k] = pack_f16x2(p0, p1);
                         pk[k + 1] = pack_f16x2(p2, p3);
                     }
-                    lr01 = fadd2(lr01, unpack2<BF16>(pk[k]));
-                    lr23 = fadd2(lr23, unpack2<BF16>(pk[k + 1]));
+                    if constexpr (BF16) {
+                        lr01 = add_bf16x2_f32x2(pk[k], lr01);
+                        lr23 = add_bf16x2_f32x2(pk[k + 1], lr23);
+                    } else {
+                        lr01 = fadd2(lr01, unpack2<BF16>(pk[k]));
+                        lr23 = fadd2(lr23, unpack2<BF16>(pk[k + 1]));
+                    }
                     le01 = fadd2(le01, make_float2(p0, p1));
                     le23 = fadd2(le23, make_float2(p2, p3));
                 }

@@ -220,6 +220,16 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+// acc + (the two bf16 halves of pk, widened): two mixed-precision adds, the
+// same fp32 results as widening first and adding
+__device__ __forceinline__ float2 add_bf16x2_f32x2(uint32_t pk, float2 acc) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %4;\n\t}\n"
+        : "=f"(lo), "=f"(hi) : "r"(pk), "f"(acc.x), "f"(acc.y));
+    return make_float2(lo, hi);
+}
+
 // Arrive once on `bar` when every tcgen05 async op issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
