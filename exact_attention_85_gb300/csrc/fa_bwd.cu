@@ -31,8 +31,10 @@
 // dK += dS^T Q; dS^T is also written to shared memory as the B operand of
 // dQ^T = K^T dS^T.  Per Q tile: MMA S^T -> softmax phase 1 (P^T) while the
 // tensor cores compute dP^T -> MMA dV += P^T dO while softmax phase 2 forms
-// dS^T -> MMA dK, then the next tile's S^T (the softmax warps start on it
-// while the tensor cores go on), then dQ^T -> read-out warps copy dQ^T out of
+// dS^T -> MMA dK (the steps of each warp's first two query chunks as soon
+// as those are written), then the next tile's S^T (the softmax warps start on
+// it while the tensor cores go on), then dQ^T (once the softmax warps have
+// also copied dS^T to shared memory) -> read-out warps copy dQ^T out of
 // tensor memory (which frees the columns for the next dP^T) and add it into
 // dQacc with fp32 atomic reductions (one 128-byte line per warp and query
 // row) while the softmax warps work on the next tile.
@@ -127,8 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *dq_free = dq_full + 1;
     uint64_t *acc_done = dq_free + 1;
     uint64_t *drain = acc_done + 1;
-    uint64_t *ds_half = drain + 1;
-    uint64_t *ds_smem = ds_half + 1;  // dS^T is in shared memory (the B operand of dQ^T)  // dS^T of every warp's first half of query chunks is in TMEM
+    uint64_t *ds_half = drain + 1;    // dS^T of every warp's first two query chunks is in TMEM
+    uint64_t *ds_smem = ds_half + 1;  // dS^T is in shared memory (the B operand of dQ^T)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
     float *ld_smem = reinterpret_cast<float *>(smem + L::OFF_LD);
