@@ -22,6 +22,9 @@ LIB = os.path.join(BUILD, "libfa.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I", os.path.join(ROOT, "include")]
+# FA_NVTX=1: NVTX ranges around the C entry points (profiler timelines)
+if os.environ.get("FA_NVTX") == "1":
+    FLAGS.append("-DFA_NVTX")
 
 
 def _nvcc() -> str:

@@ -10,6 +10,22 @@
 #include "host_util.h"
 #include "ptx.cuh"
 
+// Optional NVTX ranges around every entry point that launches work (built
+// with -DFA_NVTX, e.g. FA_NVTX=1 for build.py): a profiler timeline then
+// shows each call by name.  Off by default; header-only, nothing to link.
+#ifdef FA_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace {
+struct FaRange {
+    explicit FaRange(const char *name) { nvtxRangePushA(name); }
+    ~FaRange() { nvtxRangePop(); }
+};
+}  // namespace
+#define FA_RANGE(name) FaRange fa_range_(name)
+#else
+#define FA_RANGE(name) ((void)0)
+#endif
+
 namespace fa {
 
 // One status word per device that loads the library (module-scope device
@@ -192,17 +208,20 @@ const char *fa_status_string(fa_status_t s) {
 
 fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
                    int N, int d, int causal, float scale, fa_dtype_t dtype, void *stream) {
+    FA_RANGE("fa_fwd");
     return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, stream);
 }
 
 fa_status_t fa_fwd_f32_out(const void *q, const void *k, const void *v, float *o_f32, float *lse, int B, int Hq,
                            int Hkv, int N, int d, int causal, float scale, fa_dtype_t dtype, void *stream) {
+    FA_RANGE("fa_fwd_f32_out");
     return fwd_common(q, k, v, o_f32, lse, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, stream, nullptr,
                       true);
 }
 
 fa_status_t fa_fwd_local(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
                          int Hkv, int N, int d, int window, float scale, fa_dtype_t dtype, void *stream) {
+    FA_RANGE("fa_fwd_local");
     if (window < 1) return FA_ERR_INVALID_ARG;
     return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, 1, window, scale, dtype, stream);
 }
@@ -221,6 +240,7 @@ size_t fa_bwd_two_pass_workspace_bytes(int B, int Hq, int N, int d) {
 fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dO,
                    void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d, int causal, float scale,
                    fa_dtype_t dtype, void *workspace, size_t workspace_bytes, void *stream) {
+    FA_RANGE("fa_bwd");
     return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, false,
                       workspace, workspace_bytes, stream);
 }
@@ -229,6 +249,7 @@ fa_status_t fa_bwd_two_pass(const void *q, const void *k, const void *v, const v
                             const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d,
                             int causal, float scale, fa_dtype_t dtype, void *workspace, size_t workspace_bytes,
                             void *stream) {
+    FA_RANGE("fa_bwd_two_pass");
     return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, true,
                       workspace, workspace_bytes, stream);
 }
@@ -237,6 +258,7 @@ fa_status_t fa_bwd_local(const void *q, const void *k, const void *v, const void
                          const void *dO, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int N, int d,
                          int window, float scale, fa_dtype_t dtype, int deterministic, void *workspace,
                          size_t workspace_bytes, void *stream) {
+    FA_RANGE("fa_bwd_local");
     if (window < 1) return FA_ERR_INVALID_ARG;
     return bwd_common(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, 1, window, scale, dtype,
                       deterministic != 0, workspace, workspace_bytes, stream);
@@ -257,6 +279,7 @@ fa_status_t check_varlen(const int *cu_seqlens, int B, int max_seqlen, int total
 fa_status_t fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, const int *cu_seqlens,
                           int B, int max_seqlen, int total, int Hq, int Hkv, int d, int causal, int window,
                           float scale, fa_dtype_t dtype, void *stream) {
+    FA_RANGE("fa_fwd_varlen");
     fa_status_t s = check_varlen(cu_seqlens, B, max_seqlen, total, Hq, Hkv, d, causal, window);
     if (s != FA_OK) return s;
     const fa::SeqLayout lay{1, B, max_seqlen, total, cu_seqlens};
@@ -275,6 +298,7 @@ fa_status_t fa_bwd_varlen(const void *q, const void *k, const void *v, const voi
                           int max_seqlen, int total, int Hq, int Hkv, int d, int causal, int window, float scale,
                           fa_dtype_t dtype, int deterministic, void *workspace, size_t workspace_bytes,
                           void *stream) {
+    FA_RANGE("fa_bwd_varlen");
     fa_status_t s = check_varlen(cu_seqlens, B, max_seqlen, total, Hq, Hkv, d, causal, window);
     if (s != FA_OK) return s;
     const fa::SeqLayout lay{1, B, max_seqlen, total, cu_seqlens};
@@ -290,6 +314,7 @@ size_t fa_hadamard_quant_workspace_bytes(long rows, int d) {
 
 fa_status_t fa_hadamard_quant_fp8(const void *x_bf16, const float *signs, void *x_e4m3, float *descale, long rows,
                                   int d, void *workspace, size_t workspace_bytes, void *stream) {
+    FA_RANGE("fa_hadamard_quant_fp8");
     if (!x_bf16 || !x_e4m3 || !descale || rows < 1) return FA_ERR_INVALID_ARG;
     if (!aligned16(x_bf16) || !aligned16(x_e4m3) || (signs && !aligned16(signs))) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
@@ -304,6 +329,7 @@ fa_status_t fa_hadamard_quant_fp8(const void *x_bf16, const float *signs, void *
 fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *q_descale,
                        const float *k_descale, const float *v_descale, void *o_bf16, float *lse, int B, int Hq,
                        int Hkv, int N, int d, int causal, float scale, void *stream) {
+    FA_RANGE("fa_fwd_fp8");
     if (!q8 || !k8 || !v8 || !q_descale || !k_descale || !v_descale || !o_bf16 || !lse) return FA_ERR_INVALID_ARG;
     const void *ptrs[] = {q8, k8, v8, o_bf16, lse};
     for (const void *p : ptrs)
@@ -329,6 +355,7 @@ fa_status_t fa_get_device_status(void *stream) {
 }
 
 long long fa_probe_exp2(float *sink, int blocks, int iters, void *stream) {
+    FA_RANGE("fa_probe_exp2");
     if (!sink || !aligned16(sink) || blocks < 1 || blocks > 65535 || iters < 1 || iters > (1 << 24)) return -1;
     long long exps = 0;
     if (fa::launch_ex2_rate(sink, blocks, iters, &exps, static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -337,6 +364,7 @@ long long fa_probe_exp2(float *sink, int blocks, int iters, void *stream) {
 }
 
 fa_status_t fa_selftest_bounded_wait(int timeout_us, void *stream) {
+    FA_RANGE("fa_selftest_bounded_wait");
     if (timeout_us < 1 || timeout_us > 1000000) return FA_ERR_INVALID_ARG;
     return from_cuda(fa::launch_selftest_wait(timeout_us, static_cast<cudaStream_t>(stream)));
 }

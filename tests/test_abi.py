@@ -113,3 +113,13 @@ def test_product_path_does_not_reference_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "fa_oracle" not in text and "liboracle" not in text, f
+
+
+def test_nvtx_ranges_build(tmp_path):
+    """The optional NVTX ranges around the entry points compile (FA_NVTX)."""
+    from exact_attention_85_gb300 import build
+    import subprocess
+    src = os.path.join(ROOT, "exact_attention_85_gb300", "csrc", "fa_api.cu")
+    cmd = [build._nvcc(), *build.ARCH, *build.FLAGS, "-DFA_NVTX", "-c", src, "-o", str(tmp_path / "fa_api.o")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
