@@ -8,6 +8,13 @@ forward (halved for causal) and 2.5x that for the backward.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+Besides the contract keys the line carries, for the headline shape:
+``l2_hot`` (the step again without the L2 flush), ``exp2_bound`` (the exp2
+throughput probe and the exp-bound time of each direction),
+``two_pass_bwd_leg``, ``window_leg``, ``varlen_leg`` and ``fp8_leg`` (the
+deterministic backward, sliding window, packed batch and FP8 rows on their
+own workloads; each can be switched off with its ``--no-*`` flag).
+
 ``--impl reference`` times the fp64 CPU oracle (test infrastructure, the
 only other place this script runs it) on a bounded sample of the same
 workload.  Under torchrun (N > 1) every rank processes its own batch shard
