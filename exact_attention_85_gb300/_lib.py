@@ -70,7 +70,8 @@ def load():
         lib.fa_probe_exp2.restype = ctypes.c_longlong
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_local", "fa_bwd_local", "fa_fwd_varlen", "fa_bwd_varlen", "fa_bwd", "fa_bwd_two_pass", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
+        for name in ("fa_fwd", "fa_fwd_local", "fa_fwd_f32_out", "fa_bwd_local", "fa_fwd_varlen", "fa_bwd_varlen",
+                     "fa_bwd", "fa_bwd_two_pass", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
                      "fa_get_device_status", "fa_selftest_bounded_wait"):
             getattr(lib, name).restype = I
         _lib = lib
