@@ -25,7 +25,7 @@ inline int grid_group_planes(int planes, int blocks, int sms) {
 }
 
 // CTA index -> plane and rank within the plane (rank 0 starts first).
-__device__ __forceinline__ void grid_decode(int idx, int planes, int blocks, int group, int &plane, int &rank) {
+__host__ __device__ __forceinline__ void grid_decode(int idx, int planes, int blocks, int group, int &plane, int &rank) {
     const int per = group * blocks;
     const int grp = idx / per;
     const int r = idx - grp * per;
