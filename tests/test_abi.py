@@ -123,3 +123,55 @@ def test_nvtx_ranges_build(tmp_path):
     cmd = [build._nvcc(), *build.ARCH, *build.FLAGS, "-DFA_NVTX", "-c", src, "-o", str(tmp_path / "fa_api.o")]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr[-2000:]
+
+
+def test_local_and_two_pass_argument_validation(lib):
+    fwd = [FAKE] * 5 + [1, 2, 1, 16, 128]
+    assert lib.fa_fwd_local(*fwd, 0, 0.1, 1, None) == 1           # window < 1
+    assert lib.fa_fwd_local(*fwd, -3, 0.1, 1, None) == 1
+    assert lib.fa_fwd_local(*([None] + fwd[1:]), 4, 0.1, 1, None) == 1
+    assert lib.fa_fwd_local(*(fwd[:9] + [96]), 4, 0.1, 1, None) == 2
+    ws2 = lib.fa_bwd_two_pass_workspace_bytes(1, 2, 16, 128)
+    assert ws2 == 256                                             # D only: 32 floats, rounded up
+    assert lib.fa_bwd_two_pass_workspace_bytes(0, 2, 16, 128) == 0
+    bwd = [FAKE] * 9 + [1, 2, 1, 16, 128]
+    assert lib.fa_bwd_two_pass(*bwd, 0, 0.1, 1, None, ws2, None) == 3
+    assert lib.fa_bwd_two_pass(*bwd, 0, 0.1, 1, FAKE, ws2 - 1, None) == 3
+    assert lib.fa_bwd_two_pass(*([FAKE + 2] + bwd[1:]), 0, 0.1, 1, FAKE, ws2, None) == 1
+    assert lib.fa_bwd_two_pass(*bwd, 0, 0.1, 5, FAKE, ws2, None) == 1   # unknown dtype
+    ws1 = lib.fa_bwd_workspace_bytes(1, 2, 16, 128)
+    assert lib.fa_bwd_local(*bwd, 0, 0.1, 1, 0, FAKE, ws1, None) == 1   # window < 1
+    # the deterministic variant needs D only; the atomic one also the dQ accumulator
+    assert lib.fa_bwd_local(*bwd, 4, 0.1, 1, 0, FAKE, ws2, None) == 3
+    assert lib.fa_bwd_local(*bwd, 4, float("inf"), 1, 1, FAKE, ws2, None) == 1
+
+
+def test_varlen_argument_validation(lib):
+    cu = FAKE
+    # (q, k, v, o, lse, cu_seqlens, B, max_seqlen, total, Hq, Hkv, d, causal, window, scale, dtype, stream)
+    def fwd(**kw):
+        a = dict(q=FAKE, cu=cu, B=2, max_seqlen=16, total=24, Hq=2, Hkv=1, d=128, causal=1, window=0,
+                 scale=0.1, dtype=1)
+        a.update(kw)
+        return lib.fa_fwd_varlen(a["q"], FAKE, FAKE, FAKE, FAKE, a["cu"], a["B"], a["max_seqlen"], a["total"],
+                                 a["Hq"], a["Hkv"], a["d"], a["causal"], a["window"], a["scale"], a["dtype"],
+                                 None)
+    assert fwd(cu=None) == 1
+    assert fwd(cu=FAKE + 2) == 1            # offsets not 4-byte aligned
+    assert fwd(B=0) == 1
+    assert fwd(max_seqlen=0) == 1
+    assert fwd(total=0) == 1
+    assert fwd(window=-1) == 1
+    assert fwd(window=4, causal=0) == 1     # a window needs the causal mask
+    assert fwd(Hq=3, Hkv=2) == 1
+    assert fwd(d=32) == 2
+    assert fwd(total=1 << 24, Hq=1 << 4) == 2   # total * H * d beyond 2^31 - 1
+    assert fwd(q=FAKE + 8) == 1
+    for det in (0, 1):
+        need = lib.fa_bwd_varlen_workspace_bytes(24, 2, 128, det)
+        assert need == 256 + (0 if det else 24 * 2 * 128 * 4)
+        args = [FAKE] * 9 + [cu, 2, 16, 24, 2, 1, 128, 1, 0, 0.1, 1, det]
+        assert lib.fa_bwd_varlen(*args, FAKE, need - 1, None) == 3
+        assert lib.fa_bwd_varlen(*args, FAKE + 64, need, None) == 3   # not 256-aligned
+        assert lib.fa_bwd_varlen(*(args[:9] + [None] + args[10:]), FAKE, need, None) == 1
+    assert lib.fa_bwd_varlen_workspace_bytes(0, 2, 128, 0) == 0
