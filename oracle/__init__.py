@@ -21,6 +21,10 @@ Functions and the passages they follow:
 * ``hadamard`` / ``e4m3_round`` -- random-sign Hadamard rotation and the OCP
   e4m3 grid used by the FP8 path (FlashAttention-3 summary page, FP8 and
   incoherent processing section).
+* ``mx_e4m3`` / ``fp8_bwd_model`` -- block-scaled e4m3 quantisation (one
+  power-of-two scale per 32 entries along a product's reduction axis) and a
+  model of the backward with its five products on quantised operands: the
+  numerical basis of an FP8 backward (the pages report the FP8 forward only).
 
 Every function is pinned by the CPU tests in ``tests/test_oracle.py`` against
 closed forms, finite differences, library routines and the page's two-block
@@ -221,6 +225,106 @@ def fp8_reference(q, k, v, signs, causal: bool, scale: float):
     unpinned by the pages, which report only a 2.6x ratio.
     """
     return attention_fwd(*fp8_dequantized(q, k, v, signs), causal, scale)
+
+
+def mx_e4m3(x, axis: int, block: int = 32):
+    """Block-scaled e4m3 quantisation along ``axis``: every run of ``block``
+    consecutive entries along that axis (the last run may be shorter) shares
+    one power-of-two scale 2^e, the smallest with max|x| <= 448 * 2^e, so no
+    entry saturates; each entry becomes 2^e * e4m3(x / 2^e).  A block of
+    zeros keeps scale 1.  Exponents are limited to the 8-bit exponent-only
+    scale range [-127, 127].
+
+    This is the operand format of a block-scaled FP8 product: one scale per
+    32 entries along the product's reduction axis (the blocked counterpart of
+    the per-tensor scaling in the FlashAttention-3 summary page, FP8 and
+    incoherent processing section).  Returns (dequantised x, exponents), the
+    exponents with ``axis`` shortened to ceil(n / block)."""
+    x = _f64(x)
+    xm = np.moveaxis(x, axis, -1)
+    n = xm.shape[-1]
+    nb = -(-n // block)
+    out = np.empty_like(xm)
+    exps = np.zeros(xm.shape[:-1] + (nb,), dtype=np.int64)
+    for j in range(nb):
+        blk = xm[..., j * block:(j + 1) * block]
+        amax = np.abs(blk).max(axis=-1)
+        e = np.zeros(amax.shape, dtype=np.int64)
+        nz = amax > 0
+        if nz.any():
+            _, ex = np.frexp(amax[nz] / 448.0)   # first guess, then exact fix-up
+            ev = ex.astype(np.int64)
+            ev = np.where(amax[nz] > np.ldexp(448.0, ev), ev + 1, ev)
+            ev = np.where(amax[nz] <= np.ldexp(448.0, ev - 1), ev - 1, ev)
+            e[nz] = np.clip(ev, -127, 127)
+        sc = np.ldexp(1.0, e)[..., None]
+        out[..., j * block:(j + 1) * block] = e4m3_round(blk / sc) * sc
+        exps[..., j] = e
+    return np.moveaxis(out, -1, axis), np.moveaxis(exps, -1, axis)
+
+
+def fp8_bwd_model(q, k, v, dO, causal: bool, scale: float, mode="mx32", signs=None,
+                  products=("S", "dP", "dV", "dK", "dQ")):
+    """Model of an FP8 backward: the gradients of ``attention_bwd`` with the
+    operands of all five products of the backward step list (blog.csdn.net
+    FlashAttention-2 page, 3.1.2: S = Q K^T, dP = dO V^T, dV = P^T dO,
+    dK = dS^T Q, dQ = dS K) quantised to e4m3 before an exact fp64 product.
+
+    mode: None -- no quantisation (equals ``attention_bwd``);
+          "mx32" -- ``mx_e4m3`` along each product's reduction axis (d for S
+          and dP, queries for dV and dK, keys for dQ);
+          "tensor" -- one scale per operand matrix, sigma = amax / 448 of that
+          matrix (the most favourable per-tensor choice: a kernel knows the
+          amax of P or dS only after forming them).
+    P = exp(S - L) uses L of the same quantised S, D = rowsum(dO o O) with
+    O = P V; ``signs`` rotates Q and K by the random-sign Hadamard first and
+    rotates dQ, dK back (the rotation is orthogonal, so mode None stays
+    exact).  ``products`` names the products that take quantised operands
+    (the others stay exact), to attribute the error.  Returns (dQ, dK, dV)
+    in fp64."""
+    q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
+    B, Hq, Hkv, N, d = _shapes(q, k)
+    G = Hq // Hkv
+
+    unknown = set(products) - {"S", "dP", "dV", "dK", "dQ"}
+    if unknown:
+        raise ValueError(f"unknown products {sorted(unknown)}")
+
+    def qz(x, axis, product):
+        if mode is None or product not in products:
+            return x
+        if mode == "mx32":
+            return mx_e4m3(x, axis)[0]
+        if mode == "tensor":
+            sigma = np.abs(x).max() / 448.0
+            return x if sigma == 0.0 else e4m3_round(x / sigma) * sigma
+        raise ValueError(f"unknown mode {mode!r}")
+
+    if signs is not None:
+        q, k = hadamard(q, signs), hadamard(k, signs)
+    keep = np.tril(np.ones((N, N), dtype=bool)) if causal else np.ones((N, N), dtype=bool)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            Q, K, V, dOh = q[b, h], k[b, g], v[b, g], dO[b, h]
+            S = scale * (qz(Q, 1, "S") @ qz(K, 1, "S").T)
+            S = np.where(keep, S, -np.inf)
+            m = S.max(axis=1, keepdims=True)
+            L = m + np.log(np.exp(S - m).sum(axis=1, keepdims=True))
+            P = np.exp(S - L)
+            D = (dOh * (P @ V)).sum(axis=1, keepdims=True)
+            dP = qz(dOh, 1, "dP") @ qz(V, 1, "dP").T
+            dS = P * (dP - D)
+            dv[b, g] += qz(P, 0, "dV").T @ qz(dOh, 0, "dV")
+            dk[b, g] += scale * (qz(dS, 0, "dK").T @ qz(Q, 0, "dK"))
+            dq[b, h] = scale * (qz(dS, 1, "dQ") @ qz(K, 0, "dQ"))
+    if signs is not None:
+        s = _f64(signs).reshape(d)
+        dq, dk = hadamard(dq) * s, hadamard(dk) * s
+    return dq, dk, dv
 
 
 def _segments(cu):
