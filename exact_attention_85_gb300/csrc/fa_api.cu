@@ -129,12 +129,14 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-fa_status_t check_shape(int B, int Hq, int Hkv, int N, int d, float scale) {
+// rows: rows of one head's tensors, B * N dense or `total` packed (a packed
+// batch holds far fewer rows than B * max_seqlen when its lengths differ)
+fa_status_t check_shape(int B, int Hq, int Hkv, int N, int d, float scale, long long rows) {
     if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
     if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    const long long elems = (long long)B * Hq * N * d;
+    const long long elems = rows * Hq * d;  // the largest tensor (Hq >= Hkv)
     if (elems > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
     // 1-D grid of (Q tiles x heads x batch) CTAs
     if ((long long)((N + 127) / 128) * B * Hq > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
@@ -153,7 +155,7 @@ fa_status_t fwd_common(const void *q, const void *k, const void *v, void *o, flo
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
-    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
+    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale, packed ? packed->total : (long long)B * N);
     if (s != FA_OK) return s;
     fa::SeqLayout lay{0, B, N, B * N, nullptr};
     if (packed) lay = *packed;
@@ -172,7 +174,7 @@ fa_status_t bwd_common(const void *q, const void *k, const void *v, const void *
     for (const void *p : ptrs)
         if (!aligned16(p)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
-    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
+    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale, packed ? packed->total : (long long)B * N);
     if (s != FA_OK) return s;
     fa::SeqLayout lay{0, B, N, B * N, nullptr};
     if (packed) lay = *packed;
@@ -334,7 +336,7 @@ fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8, const flo
     const void *ptrs[] = {q8, k8, v8, o_bf16, lse};
     for (const void *p : ptrs)
         if (!aligned16(p)) return FA_ERR_INVALID_ARG;
-    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale);
+    fa_status_t s = check_shape(B, Hq, Hkv, N, d, scale, (long long)B * N);
     if (s != FA_OK) return s;
     if (d != 128) return FA_ERR_UNSUPPORTED;  // one 128-byte swizzle atom per e4m3 row
     fa::Fp8FwdArgs a{q8, k8, v8, q_descale, k_descale, v_descale, o_bf16, lse, B, Hq, Hkv, N, d,

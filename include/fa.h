@@ -20,7 +20,8 @@
  * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  All
  *           compute entry points are asynchronous on that stream.
  * Sizes.    1 <= N; d in {64, 128}; Hq % Hkv == 0; B, Hq, Hkv >= 1; the
- *           element count B*Hq*N*d must fit in 2^31 - 1 per tensor.
+ *           element count B*Hq*N*d must fit in 2^31 - 1 per tensor (packed
+ *           batches: total*Hq*d, whatever B * max_seqlen is).
  * Errors.   Invalid arguments are reported before anything is launched
  *           (FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_WORKSPACE) and
  *           leave every output untouched.  A failed launch returns

@@ -175,3 +175,18 @@ def test_varlen_argument_validation(lib):
         assert lib.fa_bwd_varlen(*args, FAKE + 64, need, None) == 3   # not 256-aligned
         assert lib.fa_bwd_varlen(*(args[:9] + [None] + args[10:]), FAKE, need, None) == 1
     assert lib.fa_bwd_varlen_workspace_bytes(0, 2, 128, 0) == 0
+
+
+def test_packed_batch_size_limit_counts_packed_rows(lib):
+    """A packed batch is sized by its total rows, not by B * max_seqlen: 64
+    sequences with one of 32768 rows and 3000 rows in all pass the size check
+    (and here stop at the undersized workspace, before any launch)."""
+    B, max_seqlen, total, Hq, d = 64, 32768, 3000, 16, 128
+    assert B * max_seqlen * Hq * d > 2 ** 31                      # the old, dense-shaped count
+    need = lib.fa_bwd_varlen_workspace_bytes(total, Hq, d, 0)
+    args = [FAKE] * 9 + [FAKE, B, max_seqlen, total, Hq, Hq, d, 1, 0, 0.1, 1, 0]
+    assert lib.fa_bwd_varlen(*args, FAKE, need - 256, None) == 3
+    # more packed rows than the limit allows are still refused
+    big = 2 ** 31 // (Hq * d) + 1
+    args_big = [FAKE] * 9 + [FAKE, B, max_seqlen, big, Hq, Hq, d, 1, 0, 0.1, 1, 0]
+    assert lib.fa_bwd_varlen(*args_big, FAKE, 1 << 40, None) == 2
