@@ -298,8 +298,11 @@ fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8,
 
 /*
  * Reads and clears the current device's status word, which kernels set when
- * a bounded wait runs out.  Synchronises `stream` first.  Returns FA_OK or
- * FA_ERR_TIMEOUT (or FA_ERR_CUDA if the copy itself fails).
+ * a bounded wait runs out or when packed sequence offsets read on the device
+ * break the rules of fa_fwd_varlen.  Synchronises `stream` first.  Returns
+ * FA_OK, FA_ERR_TIMEOUT (a wait ran out; it wins if both happened),
+ * FA_ERR_INVALID_ARG (bad device-side offsets), or FA_ERR_CUDA if the copy
+ * itself fails.
  */
 fa_status_t fa_get_device_status(void *stream);
 
