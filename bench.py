@@ -83,7 +83,7 @@ def _src_sha(files):
 def _traffic(kernel: str, files):
     """DRAM bytes per launch from a committed ncu summary, if the kernel
     source is unchanged since that capture; else None."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = os.path.join(ROOT, "profiles", "dram_traffic_bf16_b4_h16_n8k_causal.json")
     try:
         with open(path) as f:
             t = json.load(f)[kernel]
