@@ -26,7 +26,7 @@
  *   dS = P o (dP - D), dQ = scale * dS K, dK = scale * dS^T Q.
  * The scale factor is carried by the chain rule because the forward scores are
  * scale * Q K^T (section 6.1 of the Vietnamese page divides by sqrt(d)); the
- * blog's backward list omits it, which is the reading recorded for this build.
+ * blog's backward list omits it, and the chain rule puts it back.
  * Grouped-query heads: query head h reads key/value head h / (Hq / Hkv), and
  * dK, dV sum over the query heads of a group ("multi-query and grouped-query
  * attention" paragraph at the end of the blog.csdn.net page).
