@@ -248,3 +248,25 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
         except AssertionError:
             caught += 1
     assert caught > 0, f"no pin fails for {name}"
+
+
+# ------------------------------------------- per-tensor model of the forward
+
+def test_fp8_dequantized_matches_brute_force_per_tensor_scale():
+    """The FP8 forward's input model: Q and K rotated (here by an explicit
+    signed Sylvester matrix built in the test), then every tensor scaled by
+    sigma = amax / 448, rounded to the nearest e4m3 value (brute force over the
+    grid) and scaled back; V is not rotated."""
+    rng = np.random.default_rng(17)
+    d = 16
+    q, k, v = (rng.standard_normal((1, 2, 24, d)) * s for s in (3.0, 0.2, 50.0))
+    # a power-of-two change of sigma moves only values in e4m3's subnormal
+    # range (|x / sigma| < 2^-6), so V gets a few of those
+    v[0, 0, 0, :4] = np.abs(v).max() * np.array([1e-5, 2.5e-5, -3e-6, 1.7e-5])
+    signs = np.where(rng.random(d) < 0.5, -1.0, 1.0)
+    H = np.array([[(-1.0) ** bin(i & j).count("1") for j in range(d)] for i in range(d)]) / np.sqrt(d)
+    qm, km, vm = oracle.fp8_dequantized(q, k, v, signs)
+    for got, x in ((qm, (q * signs) @ H), (km, (k * signs) @ H), (vm, v)):
+        sigma = np.abs(x).max() / 448.0
+        assert np.abs(x / sigma).max() == pytest.approx(448.0, rel=1e-15)
+        np.testing.assert_allclose(got, _nearest(x / sigma) * sigma, rtol=0, atol=1e-12 * np.abs(x).max())
