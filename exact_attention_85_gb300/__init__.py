@@ -15,7 +15,8 @@ import math
 
 from . import _lib
 
-__all__ = ["attention_fwd", "attention_bwd", "hadamard_quant_fp8", "attention_fwd_fp8"]
+__all__ = ["attention_fwd", "attention_bwd", "attention_fwd_varlen", "attention_bwd_varlen",
+           "hadamard_quant_fp8", "attention_fwd_fp8"]
 
 
 def _default_scale(d: int) -> float:
@@ -63,6 +64,49 @@ def attention_bwd(q, k, v, o, lse, dO, causal: bool = False, scale: float | None
     else:
         fn = _lib.fa_bwd_two_pass if deterministic else _lib.fa_bwd
         fn(q, k, v, o, lse, dO, dq, dk, dv, causal, sc, workspace, stream)
+    return dq, dk, dv
+
+
+def attention_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int | None = None, causal: bool = False,
+                         scale: float | None = None, window: int | None = None, stream=None):
+    """Packed batch: sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1 of
+    q [total,Hq,d] and k/v [total,Hkv,d] and attends only within itself.
+    ``cu_seqlens`` is an int32 tensor [B+1] on the device.  Returns
+    (O [total,Hq,d], LSE [Hq,total] fp32).  ``max_seqlen`` defaults to the
+    longest sequence (read back from the device once)."""
+    import torch
+    total, Hq, d = q.shape
+    if max_seqlen is None:
+        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item())
+    if window is not None and not causal:
+        raise ValueError("a sliding window is defined on top of the causal mask")
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, total), dtype=torch.float32, device=q.device)
+    sc = _default_scale(d) if scale is None else scale
+    _lib.fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen, causal, sc, window or 0, stream)
+    return o, lse
+
+
+def attention_bwd_varlen(q, k, v, o, lse, dO, cu_seqlens, max_seqlen: int | None = None, causal: bool = False,
+                         scale: float | None = None, window: int | None = None, deterministic: bool = False,
+                         workspace=None, stream=None):
+    """Gradients (dQ [total,Hq,d], dK, dV [total,Hkv,d]) of a packed batch
+    from the forward's O and LSE and the incoming dO; arguments as
+    ``attention_fwd_varlen``.  ``deterministic=True`` forms dQ in a second
+    pass instead of by atomic addition."""
+    import torch
+    total, Hq, d = q.shape
+    if max_seqlen is None:
+        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item())
+    if window is not None and not causal:
+        raise ValueError("a sliding window is defined on top of the causal mask")
+    if workspace is None:
+        workspace = torch.empty(_lib.fa_bwd_varlen_workspace_bytes(total, Hq, d, deterministic),
+                                dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    sc = _default_scale(d) if scale is None else scale
+    _lib.fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens, max_seqlen, causal, sc, deterministic,
+                       workspace, window or 0, stream)
     return dq, dk, dv
 
 

@@ -190,3 +190,33 @@ def test_packed_batch_size_limit_counts_packed_rows(lib):
     big = 2 ** 31 // (Hq * d) + 1
     args_big = [FAKE] * 9 + [FAKE, B, max_seqlen, big, Hq, Hq, d, 1, 0, 0.1, 1, 0]
     assert lib.fa_bwd_varlen(*args_big, FAKE, 1 << 40, None) == 2
+
+
+def test_packed_batch_wrappers_marshal_arguments(monkeypatch):
+    """The public packed-batch wrappers only allocate outputs and pass them on:
+    checked on CPU tensors against a stand-in for the binding that records
+    its arguments (nothing is launched)."""
+    import torch
+    import exact_attention_85_gb300 as fa
+    from exact_attention_85_gb300 import _lib
+
+    calls = {}
+    monkeypatch.setattr(_lib, "fa_fwd_varlen", lambda *a: calls.setdefault("fwd", a))
+    monkeypatch.setattr(_lib, "fa_bwd_varlen", lambda *a: calls.setdefault("bwd", a))
+    monkeypatch.setattr(_lib, "fa_bwd_varlen_workspace_bytes", lambda total, Hq, d, det: 256 + (0 if det else 99))
+    total, Hq, Hkv, d = 10, 4, 2, 64
+    q = torch.zeros(total, Hq, d, dtype=torch.bfloat16)
+    k = v = torch.zeros(total, Hkv, d, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 3, 3, 10], dtype=torch.int32)
+    o, lse = fa.attention_fwd_varlen(q, k, v, cu, causal=True, window=5)
+    a = calls["fwd"]
+    assert a[0] is q and a[3] is o and a[4] is lse and a[5] is cu
+    assert o.shape == q.shape and o.dtype == q.dtype and lse.shape == (Hq, total) and lse.dtype == torch.float32
+    assert a[6] == 7 and a[7] is True and a[8] == pytest.approx(d ** -0.5) and a[9] == 5   # max_seqlen, causal, scale, window
+    dq, dk, dv = fa.attention_bwd_varlen(q, k, v, o, lse, q, cu, causal=False, deterministic=True)
+    b = calls["bwd"]
+    assert b[6] is dq and b[7] is dk and b[8] is dv and b[9] is cu and b[10] == 7
+    assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
+    assert b[13] is True and b[14].numel() == 256 and b[15] == 0                           # deterministic, workspace, window
+    with pytest.raises(ValueError):
+        fa.attention_fwd_varlen(q, k, v, cu, causal=False, window=3)
