@@ -220,3 +220,46 @@ def test_packed_batch_wrappers_marshal_arguments(monkeypatch):
     assert b[13] is True and b[14].numel() == 256 and b[15] == 0                           # deterministic, workspace, window
     with pytest.raises(ValueError):
         fa.attention_fwd_varlen(q, k, v, cu, causal=False, window=3)
+
+
+def test_dense_and_fp8_wrappers_marshal_arguments(monkeypatch):
+    """The dense and FP8 wrappers pick the entry point the arguments ask for
+    and allocate outputs of the right shape and type (CPU tensors, stand-in
+    binding, nothing launched)."""
+    import torch
+    import exact_attention_85_gb300 as fa
+    from exact_attention_85_gb300 import _lib
+
+    calls = []
+    for name in ("fa_fwd", "fa_fwd_local", "fa_bwd", "fa_bwd_two_pass", "fa_bwd_local", "fa_hadamard_quant_fp8",
+                 "fa_fwd_fp8"):
+        monkeypatch.setattr(_lib, name, lambda *a, _n=name: calls.append((_n, a)))
+    monkeypatch.setattr(_lib, "fa_bwd_workspace_bytes", lambda *a: 1000)
+    monkeypatch.setattr(_lib, "fa_bwd_two_pass_workspace_bytes", lambda *a: 300)
+    monkeypatch.setattr(_lib, "fa_hadamard_quant_workspace_bytes", lambda *a: 256)
+    B, Hq, Hkv, N, d = 2, 4, 2, 8, 128
+    q = torch.zeros(B, Hq, N, d, dtype=torch.float16)
+    k = v = torch.zeros(B, Hkv, N, d, dtype=torch.float16)
+    o, lse = fa.attention_fwd(q, k, v, causal=True)
+    assert calls[-1][0] == "fa_fwd" and calls[-1][1][5] is True and calls[-1][1][6] == pytest.approx(d ** -0.5)
+    assert o.shape == q.shape and o.dtype == q.dtype and lse.shape == (B, Hq, N) and lse.dtype == torch.float32
+    fa.attention_fwd(q, k, v, causal=True, scale=0.5, window=3)
+    assert calls[-1][0] == "fa_fwd_local" and calls[-1][1][5:7] == (3, 0.5)
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, lse, q, causal=True)
+    n, a = calls[-1]
+    assert n == "fa_bwd" and a[6] is dq and a[7] is dk and a[8] is dv and a[11].numel() == 1000
+    assert dk.shape == k.shape and dv.shape == v.shape
+    fa.attention_bwd(q, k, v, o, lse, q, causal=False, deterministic=True)
+    assert calls[-1][0] == "fa_bwd_two_pass" and calls[-1][1][11].numel() == 300
+    fa.attention_bwd(q, k, v, o, lse, q, causal=True, deterministic=True, window=4)
+    assert calls[-1][0] == "fa_bwd_local" and calls[-1][1][9] == 4 and calls[-1][1][11] is True
+    with pytest.raises(ValueError):
+        fa.attention_bwd(q, k, v, o, lse, q, causal=False, window=4)
+    x = torch.zeros(3, 5, d, dtype=torch.bfloat16)
+    x8, desc = fa.hadamard_quant_fp8(x)
+    assert calls[-1][0] == "fa_hadamard_quant_fp8" and x8.dtype == torch.float8_e4m3fn and x8.shape == x.shape
+    assert desc.shape == (1,) and desc.dtype == torch.float32
+    q8 = torch.zeros(B, Hq, N, d, dtype=torch.float8_e4m3fn)
+    o8, lse8 = fa.attention_fwd_fp8(q8, q8[:, :Hkv], q8[:, :Hkv], desc, desc, desc, causal=True)
+    assert calls[-1][0] == "fa_fwd_fp8" and o8.dtype == torch.bfloat16 and o8.shape == q8.shape
+    assert lse8.shape == (B, Hq, N)
