@@ -263,3 +263,53 @@ def test_dense_and_fp8_wrappers_marshal_arguments(monkeypatch):
     o8, lse8 = fa.attention_fwd_fp8(q8, q8[:, :Hkv], q8[:, :Hkv], desc, desc, desc, causal=True)
     assert calls[-1][0] == "fa_fwd_fp8" and o8.dtype == torch.bfloat16 and o8.shape == q8.shape
     assert lse8.shape == (B, Hq, N)
+
+
+def test_binding_marshals_shapes_dtypes_and_errors(monkeypatch):
+    """The ctypes layer passes pointers, sizes, element-type codes and
+    workspace bytes as the header orders them, and turns a status other
+    than FA_OK into FAError (stand-in library, CPU tensors, nothing runs)."""
+    import torch
+    from exact_attention_85_gb300 import _lib
+
+    class Fake:
+        def __init__(self):
+            self.calls, self.ret = [], 0
+
+        def __getattr__(self, name):
+            if name == "fa_status_string":
+                return lambda s: b"FA_ERR_UNSUPPORTED" if s == 2 else b"?"
+            return lambda *a: (self.calls.append((name, a)), self.ret)[1]
+
+    fake = Fake()
+    monkeypatch.setattr(_lib, "load", lambda: fake)
+    B, Hq, Hkv, N, d = 2, 6, 3, 40, 64
+    q = torch.zeros(B, Hq, N, d, dtype=torch.bfloat16)
+    k = v = torch.zeros(B, Hkv, N, d, dtype=torch.bfloat16)
+    lse = torch.zeros(B, Hq, N)
+    _lib.fa_fwd(q, k, v, q, lse, True, 0.25, stream=7)
+    name, a = fake.calls[-1]
+    assert name == "fa_fwd" and a[0] == q.data_ptr() and a[4] == lse.data_ptr()
+    assert a[5:] == (B, Hq, Hkv, N, d, 1, 0.25, _lib.FA_BF16, 7)
+    ws = torch.zeros(300, dtype=torch.int32)
+    _lib.fa_bwd(q.half(), k, v, q, lse, q, q, k, v, False, 0.5, ws, stream=3)
+    name, a = fake.calls[-1]
+    assert a[9:] == (B, Hq, Hkv, N, d, 0, 0.5, _lib.FA_FP16, ws.data_ptr(), 1200, 3)
+    total = 33
+    qp = torch.zeros(total, Hq, d, dtype=torch.bfloat16)
+    kp = torch.zeros(total, Hkv, d, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 10, 33], dtype=torch.int32)
+    _lib.fa_bwd_varlen(qp, kp, kp, qp, lse, qp, qp, kp, kp, cu, 23, True, 0.1, True, ws, window=5, stream=1)
+    name, a = fake.calls[-1]
+    assert a[9] == cu.data_ptr() and a[10:] == (2, 23, total, Hq, Hkv, d, 1, 5, pytest.approx(0.1), _lib.FA_BF16,
+                                                1, ws.data_ptr(), 1200, 1)
+    x = torch.zeros(5, 7, 128, dtype=torch.bfloat16)
+    _lib.fa_hadamard_quant_fp8(x, None, x, lse, ws, stream=2)
+    name, a = fake.calls[-1]
+    assert a[1] is None and a[4:] == (35, 128, ws.data_ptr(), 1200, 2)
+    with pytest.raises(TypeError):
+        _lib.fa_fwd(q.float(), k, v, q, lse, True, 0.25, stream=7)
+    fake.ret = 2
+    with pytest.raises(_lib.FAError) as e:
+        _lib.fa_fwd(q, k, v, q, lse, True, 0.25, stream=7)
+    assert e.value.status == 2 and "FA_ERR_UNSUPPORTED" in str(e.value)
