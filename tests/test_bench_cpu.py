@@ -41,3 +41,25 @@ def test_visible_pairs_and_flop_counts():
     assert w.bwd_flops() == pytest.approx(2.5 * w.fwd_flops())
     t = WORKLOADS["tiny_fp16_d64_n256"]
     assert not t.causal and bench._visible_pairs(t) == t.B * t.Hq * 256 * 256
+
+
+def test_clock_summary_reads_throttle_reasons():
+    """The clock record of the timed region: median SM clock over loaded
+    samples (power above 300 W), the maximum clock, and every throttle reason
+    seen active while loaded (nvidia-smi CSV, no units)."""
+    import bench
+
+    c = bench.ClockSampler(0)
+    c.out = "\n".join([
+        "2070, 2070, 120.5, Not Active, Not Active, Not Active, Not Active",   # idle: ignored
+        "2070, 2070, 1150.0, Not Active, Not Active, Not Active, Active",
+        "1995, 2070, 1390.2, Not Active, Not Active, Not Active, Active",
+        "2055, 2070, 1201.0, Not Active, Active, Not Active, Not Active",
+        "garbage line",
+        "[N/A], 2070, 900, Not Active, Not Active, Not Active, Not Active",
+    ])
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2055.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    c.out = ""
+    assert c.summary()["reasons"] == ["unavailable"]
