@@ -63,3 +63,22 @@ def test_clock_summary_reads_throttle_reasons():
     assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
     c.out = ""
     assert c.summary()["reasons"] == ["unavailable"]
+
+
+def test_reference_arm_under_two_ranks_prints_once():
+    """Launched as two ranks (the multi-GPU form of the command), the
+    reference arm runs on rank 0 alone and prints one line; rank 1 exits 0
+    without work."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "0"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
