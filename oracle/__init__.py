@@ -198,19 +198,26 @@ def e4m3_round(x):
 def fp8_dequantized(q, k, v, signs):
     """Q, K, V as the FP8 path sees them: Q and K rotated by the random-sign
     Hadamard (if ``signs`` is not None), each tensor quantised per tensor to
-    e4m3 with sigma = amax / 448 and dequantised (fp64)."""
-    q, k, v = _f64(q), _f64(k), _f64(v)
-    if signs is not None:
-        q = hadamard(q, signs)
-        k = hadamard(k, signs)
+    e4m3 with sigma = amax / 448 and dequantised (fp64).
 
-    def qdq(x):
-        sigma = np.abs(x).max() / 448.0
-        if sigma == 0.0:
-            return x
-        return e4m3_round(x / sigma) * sigma
+    Each tensor is handled one leading slice at a time, in two passes (the
+    amax over all slices, then the rounding of each slice; the rotation and
+    the rounding are per row), so the host memory needed is the fp64 output
+    plus one slice."""
 
-    return qdq(q), qdq(k), qdq(v)
+    def qdq(x, rotate: bool):
+        def part(i):
+            return hadamard(x[i], signs) if rotate else _f64(x[i])
+
+        sigma = max(float(np.abs(part(i)).max()) for i in range(x.shape[0])) / 448.0
+        out = np.empty(tuple(x.shape), dtype=np.float64)
+        for i in range(x.shape[0]):
+            p = part(i)
+            out[i] = p if sigma == 0.0 else e4m3_round(p / sigma) * sigma
+        return out
+
+    rot = signs is not None
+    return qdq(q, rot), qdq(k, rot), qdq(v, False)
 
 
 def fp8_reference(q, k, v, signs, causal: bool, scale: float):
