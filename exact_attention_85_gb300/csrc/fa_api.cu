@@ -35,8 +35,14 @@ __device__ unsigned int g_status_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
-unsigned int *g_status_ptr[kMaxDevices];
+struct StatusSlot {
+    void *ctx;  // context the address was looked up in
+    unsigned int *addr;
+};
+StatusSlot g_status_slot[kMaxDevices];
 std::mutex g_mutex;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -102,16 +108,34 @@ bool make_tmap_tiles(CUtensorMap *map, const void *base, CUtensorMapDataType dty
                             CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+void *current_context() {
+    static CtxGetCurrentFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<CtxGetCurrentFn>(nullptr);
+        return reinterpret_cast<CtxGetCurrentFn>(f);
+    }();
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+    return ctx;
+}
+
 unsigned int *device_status_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    void *ctx = current_context();  // null before the runtime has made one current
     std::lock_guard<std::mutex> lk(g_mutex);
-    if (!g_status_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-        g_status_ptr[dev] = static_cast<unsigned int *>(p);
-    }
-    return g_status_ptr[dev];
+    StatusSlot &s = g_status_slot[dev];
+    if (s.addr != nullptr && ctx != nullptr && s.ctx == ctx) return s.addr;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || p == nullptr) return nullptr;
+    if (ctx == nullptr) ctx = current_context();  // the lookup made the context current
+    if (ctx == nullptr) return nullptr;
+    s.ctx = ctx;
+    s.addr = static_cast<unsigned int *>(p);
+    return s.addr;
 }
 
 cudaError_t launch_selftest_wait(int timeout_us, cudaStream_t st) {
@@ -353,6 +377,7 @@ fa_status_t fa_get_device_status(void *stream) {
     if (cudaMemsetAsync(p, 0, sizeof(unsigned int), st) != cudaSuccess) return FA_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
     if (host & fa::kStatusTimeout) return FA_ERR_TIMEOUT;
+    if (host & fa::kStatusBadLaunch) return FA_ERR_CUDA;
     return (host & fa::kStatusBadArgs) ? FA_ERR_INVALID_ARG : FA_OK;
 }
 

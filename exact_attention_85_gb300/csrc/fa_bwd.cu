@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     if (pad > (uint32_t)L::SLACK) {  // uniform across the CTA; nothing started yet
-        if (threadIdx.x == 0) record_timeout(p.status, 0x7FFF);
+        if (threadIdx.x == 0) record_bad_launch(p.status);
         return;
     }
     uint8_t *smem = smem_raw + pad;
@@ -759,7 +759,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     if (pad > (uint32_t)L::SLACK) {  // uniform across the CTA; nothing started yet
-        if (threadIdx.x == 0) record_timeout(p.status, 0x7FFE);
+        if (threadIdx.x == 0) record_bad_launch(p.status);
         return;
     }
     uint8_t *smem = smem_raw + pad;

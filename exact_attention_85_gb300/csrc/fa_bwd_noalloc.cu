@@ -10,17 +10,21 @@
 // lives in the library itself (a file-scope device array), so a call
 // allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
 //
-// The buffer is FA_BWD_NOALLOC_SCRATCH_BYTES long (include/fa.h).  Every
-// device that loads this part of the library holds it until the process
-// exits.  All calls on a device share it, so two calls whose kernels overlap
-// on the GPU (different streams, no ordering between them) race on it.  Each
-// call overwrites D and zeroes the dQ accumulator before using them, so the
-// contents left by an earlier call never leak into a later one.
+// The buffer is FA_BWD_NOALLOC_SCRATCH_BYTES long (include/fa.h).  It belongs
+// to this translation unit's own module, which the CUDA runtime loads -- and
+// so commits the buffer's device memory -- when the module is first used (the
+// first call on a device, under the default lazy module loading) or when the
+// library is loaded (CUDA_MODULE_LOADING=EAGER).  From then on the device
+// holds it until the process exits.  All calls on a device share it, so two
+// calls whose kernels overlap on the GPU (different streams, no ordering
+// between them) race on it.  Each call overwrites D and zeroes the dQ
+// accumulator before using them, so the contents left by an earlier call
+// never leak into a later one.
 #include <cstdint>
 #include <mutex>
 
 #include "../../include/fa.h"
-#include <cuda_runtime.h>
+#include "host_util.h"
 
 namespace {
 
@@ -32,21 +36,33 @@ constexpr size_t kScratchBytes = FA_BWD_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices];
+struct ScratchSlot {
+    void *ctx;  // context the address was looked up in
+    void *addr;
+};
+ScratchSlot g_slot[kMaxDevices];
 std::mutex g_scratch_lock;
 
-// Device address of g_bwd_scratch on the current device; looked up once per
-// device (on the first call made with that device current) and cached.
+// Device address of g_bwd_scratch on the current device.  Set-up happens on
+// the first call made with the device current: cudaGetSymbolAddress (which
+// loads this module if it is not loaded yet) with its return code checked.
+// The address is cached per device together with the context it was found
+// in, and looked up again if the device's current context changes (after a
+// cudaDeviceReset the old address no longer exists).
 void *scratch_address() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    void *ctx = fa::current_context();  // null before the runtime has made one current
     std::lock_guard<std::mutex> lk(g_scratch_lock);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) return nullptr;
-        g_scratch_addr[dev] = p;
-    }
-    return g_scratch_addr[dev];
+    ScratchSlot &s = g_slot[dev];
+    if (s.addr != nullptr && ctx != nullptr && s.ctx == ctx) return s.addr;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    if (ctx == nullptr) ctx = fa::current_context();  // the lookup made the context current
+    if (ctx == nullptr) return nullptr;
+    s.ctx = ctx;
+    s.addr = p;
+    return p;
 }
 
 }  // namespace
@@ -55,16 +71,19 @@ extern "C" fa_status_t fa_bwd_noalloc(const void *q, const void *k, const void *
                                       const float *lse, const void *dO, void *dq, void *dk, void *dv, int B,
                                       int Hq, int Hkv, int N, int d, int causal, float scale, fa_dtype_t dtype,
                                       void *stream) {
-    // Size check first: a problem too large for the built-in buffer is
-    // refused before anything touches the GPU.
-    if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-    const size_t need = fa_bwd_workspace_bytes(B, Hq, N, d);
-    if (need == 0) return FA_ERR_INVALID_ARG;
-    if (need > kScratchBytes) return FA_ERR_WORKSPACE;
+    // fa_bwd checks the workspace last, after every other argument, and
+    // launches nothing before that check: asked without a workspace it
+    // answers FA_ERR_WORKSPACE exactly when everything else is valid.  So
+    // invalid arguments are classified here exactly as fa_bwd classifies them.
+    const fa_status_t st = fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype,
+                                  nullptr, 0, stream);
+    if (st != FA_ERR_WORKSPACE) return st;
+    // a problem too large for the built-in buffer is refused before anything
+    // touches the GPU
+    if (fa_bwd_workspace_bytes(B, Hq, N, d) > kScratchBytes) return FA_ERR_WORKSPACE;
     void *scratch = scratch_address();
     if (!scratch) return FA_ERR_CUDA;
-    // Same validation and kernels as fa_bwd, with the built-in buffer as the
-    // workspace.
-    return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype, scratch,
-                  kScratchBytes, stream);
+    // the same kernels as fa_bwd, with the built-in buffer as the workspace
+    return fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, N, d, causal, scale, dtype, scratch, kScratchBytes,
+                  stream);
 }

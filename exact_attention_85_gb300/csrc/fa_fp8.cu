@@ -22,8 +22,11 @@
 // v_descale in the epilogue.  P is lifted by 2^4 before quantisation so its
 // typical values sit in e4m3's normal range; the running max moves when a
 // tile's max exceeds it by more than 4 (log2 units), so P <= 2^8 < 448.  O is
-// normalised by the sum of the quantised P it was built from (the lift
-// cancels); L uses the sum of the unquantised P.
+// normalised by a sum of the quantised P it was built from, so the lift
+// cancels; that sum is accumulated in fp16 pairs (8 values per half before it
+// is widened), whose 11-bit significand rounds it by at most about 2^-11
+// relative per add -- far below the 2^-4 rounding of P itself.  L uses the
+// fp32 sum of the unquantised P.
 #include "grid_order.cuh"
 #include "host_util.h"
 #include "ptx.cuh"
@@ -470,8 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 sl2x2 = make_float2(sl2, sl2);
             float2 le01 = make_float2(0.f, 0.f), le23 = le01;
             // the sum of the quantised P is accumulated in fp16 pairs over 32
-            // scores (at most 32 x 256: exact range, 11-bit precision) and then
-            // widened, which costs one conversion and one add per two scores
+            // scores (each half adds 8 values of at most 256: no overflow, but
+            // every add rounds to fp16's 11-bit significand, about 2^-11
+            // relative) and then widened, which costs one conversion and one
+            // add per two scores instead of widening every value
             float lr = 0.0f;
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh) {

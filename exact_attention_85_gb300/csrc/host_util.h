@@ -40,8 +40,15 @@ bool make_tmap_3d_box(CUtensorMap *map, const void *base, CUtensorMapDataType dt
 bool make_tmap_tiles(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int d, const SeqLayout &lay,
                      int heads, uint32_t rows);
 
-// Device address of this library's status word on the current device.
+// Device address of this library's status word on the current device
+// (looked up once per device and context, cached).
 unsigned int *device_status_ptr();
+
+// The CUDA context current on the calling thread (driver handle), or null if
+// none is current or the driver entry point is unavailable.  Addresses of
+// device symbols are cached per (device, context): after a cudaDeviceReset
+// the device's next primary context is a new one and the lookup is redone.
+void *current_context();
 
 struct FwdArgs {
     const void *q, *k, *v;

@@ -14,12 +14,25 @@ constexpr unsigned int kStatusTimeout = 0x80000000u;
 // the kernel then skips the affected work instead of reading out of range.
 constexpr unsigned int kStatusBadArgs = 0x40000000u;
 
+// Bit 29 marks a kernel that found its dynamic shared-memory window too far
+// from a 1024-byte boundary for its 128-byte-swizzled operand tiles; the
+// kernel then does nothing (a launch-configuration failure, not a timeout).
+constexpr unsigned int kStatusBadLaunch = 0x20000000u;
+
+// The first timeout also records its site; other bits already set (bad
+// arguments, bad launch) do not stop a timeout from being recorded.
 __device__ __forceinline__ void record_timeout(unsigned int *status, uint32_t site) {
-    if (status) atomicCAS(status, 0u, kStatusTimeout | (site & 0xFFFFu));
+    if (!status) return;
+    const unsigned int old = atomicOr(status, kStatusTimeout);
+    if (!(old & kStatusTimeout)) atomicOr(status, site & 0xFFFFu);
 }
 
 __device__ __forceinline__ void record_bad_args(unsigned int *status) {
     if (status) atomicOr(status, kStatusBadArgs);
+}
+
+__device__ __forceinline__ void record_bad_launch(unsigned int *status) {
+    if (status) atomicOr(status, kStatusBadLaunch);
 }
 
 }  // namespace fa

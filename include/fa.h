@@ -231,15 +231,24 @@ fa_status_t fa_bwd_varlen(const void *q, const void *k, const void *v,
  * only tensor pointers by its host framework or a process whose memory pool
  * is fixed up front).  The pages have no counterpart to this entry point; it
  * exists only for such callers.
- *   Arguments, layouts and results are exactly those of fa_bwd.  The
- *   workspace is a buffer of FA_BWD_NOALLOC_SCRATCH_BYTES that lives inside
- *   the library on every device that loads it, until the process exits.
- *   Problems whose fa_bwd_workspace_bytes(B, Hq, N, d) exceeds that size are
- *   refused with FA_ERR_WORKSPACE before anything touches the GPU (with
- *   d = 128 this allows B * Hq * N up to about 130,000 rows).
- *   The first call on a device (with that device current) looks up the
- *   buffer's device address once; make that first call before any stream
- *   capture.  The call allocates nothing.
+ *   Arguments, layouts and results are exactly those of fa_bwd, and invalid
+ *   arguments get the same status codes as from fa_bwd.  The workspace is a
+ *   buffer of FA_BWD_NOALLOC_SCRATCH_BYTES inside the library.  Problems
+ *   whose fa_bwd_workspace_bytes(B, Hq, N, d) exceeds that size are refused
+ *   with FA_ERR_WORKSPACE before anything touches the GPU (with d = 128 this
+ *   allows B * Hq * N up to about 130,000 rows).
+ *   When the memory is taken: the buffer's device memory is committed when
+ *   the CUDA runtime loads the part of the library that holds it -- on the
+ *   first call on a device (default lazy module loading), or when the
+ *   library is loaded (CUDA_MODULE_LOADING=EAGER, on every device the
+ *   process uses).  It is then held until the process exits.  Make the first
+ *   call on each device (with that device current) before reserving a fixed
+ *   memory pool and before any stream capture: that call also looks up the
+ *   buffer's device address, and may fail with FA_ERR_CUDA if the device has
+ *   no room left for the buffer.  Later calls allocate nothing.
+ *   The looked-up address is cached per device and CUDA context, and looked
+ *   up again if the device's current context changes (e.g. after
+ *   cudaDeviceReset).
  *   All calls on a device share the one buffer: calls whose kernels may
  *   overlap on the GPU (e.g. on unordered streams) race and give wrong
  *   results.  Each call rewrites and re-zeroes what it uses, so nothing from
@@ -298,11 +307,19 @@ fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8,
 
 /*
  * Reads and clears the current device's status word, which kernels set when
- * a bounded wait runs out or when packed sequence offsets read on the device
- * break the rules of fa_fwd_varlen.  Synchronises `stream` first.  Returns
- * FA_OK, FA_ERR_TIMEOUT (a wait ran out; it wins if both happened),
- * FA_ERR_INVALID_ARG (bad device-side offsets), or FA_ERR_CUDA if the copy
- * itself fails.
+ * a bounded wait runs out, when packed sequence offsets read on the device
+ * break the rules of fa_fwd_varlen, or when a kernel finds its shared-memory
+ * window misaligned for its tiles (it then does nothing).  Synchronises
+ * `stream` first.  Returns, in this order of precedence: FA_ERR_TIMEOUT (a
+ * wait ran out), FA_ERR_CUDA (a kernel could not use its launch
+ * configuration, or the copy of the word itself failed), FA_ERR_INVALID_ARG
+ * (bad device-side offsets), else FA_OK.
+ *   There is ONE status word per device, shared by every caller, thread and
+ *   stream of the process, and this call clears it for all of them.  With
+ *   several streams or callers in flight, a status read on one stream may
+ *   report a condition raised by work on another (and that other caller's
+ *   later read then sees FA_OK).  Callers that need to attribute a failure
+ *   must serialise their work and their reads of the status word.
  */
 fa_status_t fa_get_device_status(void *stream);
 
