@@ -13,7 +13,10 @@ Besides the contract keys the line carries, for the headline shape:
 throughput probe and the exp-bound time of each direction),
 ``two_pass_bwd_leg``, ``window_leg``, ``varlen_leg`` and ``fp8_leg`` (the
 deterministic backward, sliding window, packed batch and FP8 rows on their
-own workloads; each can be switched off with its ``--no-*`` flag).
+own workloads), and ``configs_leg`` (forward and backward of the tiny fp16,
+training, long-context and grouped-query workloads; the fp64 oracle's host
+time on a bounded sample of each is in ``cpu_baseline.per_workload``); each
+can be switched off with its ``--no-*`` flag.
 
 ``--impl reference`` times the fp64 CPU oracle (test infrastructure, the
 only other place this script runs it) on a bounded sample of the same
@@ -51,6 +54,8 @@ def _args():
     ap.add_argument("--no-window", action="store_true", help="skip the sliding-window leg")
     ap.add_argument("--no-varlen", action="store_true", help="skip the packed variable-length leg")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 leg (outlier workload)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload legs (tiny, training, long-context and grouped-query shapes)")
     return ap.parse_args()
 
 
@@ -276,6 +281,8 @@ def run_ours(a):
         result["varlen_leg"] = _varlen_leg(a, dev, stream, peaks, flush)
     if not a.no_fp8 and a.workload is None:
         result["fp8_leg"] = _fp8_leg(a, dev, stream, peaks)
+    if not a.no_configs and a.workload is None:
+        result["configs_leg"] = _configs_leg(a, dev, stream, peaks, flush)
     if not a.no_e2e:
         result["e2e"] = _e2e(a, w, host, dev, stream, has_bwd, ws)
     if rank == 0 and ws == 1 and not a.no_cpu:
@@ -577,6 +584,67 @@ def _fp8_leg(a, dev, stream, peaks):
             "launches_per_step": 3 * 3 + 1}
 
 
+CONFIG_LEGS = ("tiny_fp16_d64_n256", "train_bf16_b8_h16_n2k_causal", "long_bf16_b1_h16_n16k_causal",
+               "gqa_bf16_b4_hq32_hkv8_n4k_causal")
+
+
+def _configs_leg(a, dev, stream, peaks, flush):
+    """Forward and backward (fa_fwd, fa_bwd) of each workload in CONFIG_LEGS,
+    timed like the step (CUDA events per call, L2 flushed between steps).
+    The fp64 oracle's host time for each of them is in
+    cpu_baseline.per_workload."""
+    import torch
+
+    from exact_attention_85_gb300 import _lib
+    from exact_attention_85_gb300.inputs import WORKLOADS, make_inputs
+
+    out = {}
+    for name in CONFIG_LEGS:
+        w = WORKLOADS[name]
+        host = make_inputs(w, with_grad=True)
+        q, k, v, dO = (host[n].to(dev).contiguous() for n in ("q", "k", "v", "dO"))
+        B, Hq, N, d = q.shape
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsb = torch.empty(_lib.fa_bwd_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device=dev)
+
+        def fwd():
+            _lib.fa_fwd(q, k, v, o, lse, w.causal, w.scale, stream)
+
+        def bwd():
+            _lib.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, w.causal, w.scale, wsb, stream)
+
+        for _ in range(max(3, a.warmup)):
+            fwd()
+            bwd()
+            flush.zero_()
+        torch.cuda.synchronize()
+        steps = max(3, min(a.steps, 20))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            bwd()
+            ev[i][2].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        if _lib.fa_get_device_status(stream) != _lib.FA_OK:
+            raise RuntimeError(f"a bounded device wait ran out during the {name} leg")
+        f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        b_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        ftf = w.fwd_flops() / (f_ms * 1e-3) / 1e12
+        btf = w.bwd_flops() / (b_ms * 1e-3) / 1e12
+        leg = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "dtype": w.dtype, "causal": w.causal,
+               "fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4), "fwd_tflops": round(ftf, 1),
+               "bwd_tflops": round(btf, 1), "fwd_frac_of_peak": round(ftf / peaks["bf16_tflops"], 4),
+               "bwd_frac_of_peak": round(btf / peaks["bf16_tflops"], 4), "launches_per_step": 4}
+        out[name] = leg
+        del q, k, v, dO, o, lse, dq, dk, dv, wsb
+    return out
+
+
 def _e2e(a, w, host, dev, stream, has_bwd, ws):
     """Same metric through the public API with pinned host buffers: every step
     copies Q, K, V, dO in and O, dQ, dK, dV out inside the timed region.  The
@@ -703,7 +771,26 @@ def _cpu_baseline(w, host, budget_s: float):
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
             "sample": f"fp64 oracle forward+backward of {n} (batch, kv-head) group(s) of {w.name} at full "
                       f"N={w.N}, {secs:.1f} s, OpenMP over {threads} host threads",
-            "single_thread": _cpu_single_thread_small()}
+            "single_thread": _cpu_single_thread_small(),
+            "per_workload": _cpu_per_workload()}
+
+
+def _cpu_per_workload():
+    """The oracle (all host threads) on a bounded sample of each workload of
+    the per-workload legs: one (batch, kv-head) group at full N, or the whole
+    workload when it is that small."""
+    from exact_attention_85_gb300.inputs import WORKLOADS, make_inputs
+
+    out = {}
+    for name in CONFIG_LEGS:
+        w = WORKLOADS[name]
+        host = make_inputs(w, with_grad=True)
+        groups = w.B * w.Hkv if w.N <= 256 else 1
+        secs, flops = _cpu_sample(w, host, groups)
+        out[name] = {"tflops": round(flops / secs / 1e12, 6), "seconds": round(secs, 3),
+                     "cores": os.cpu_count() or 1,
+                     "sample": f"fp64 forward+backward of {groups} (batch, kv-head) group(s) at full N={w.N}"}
+    return out
 
 
 def run_reference(a):

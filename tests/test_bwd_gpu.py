@@ -75,20 +75,38 @@ def test_bwd_repeatable_within_tolerance(cuda_lib):
     assert rel < 1e-3
 
 
-@pytest.mark.parametrize("name", ["train_bf16_b8_h16_n2k_causal", "long_bf16_b1_h16_n16k_causal",
-                                  "gqa_bf16_b4_hq32_hkv8_n4k_causal", HEADLINE])
-def test_bwd_full_size_sampled_group(cuda_lib, name):
-    """Full-size launch; the oracle checks one (batch, kv-head) group entirely
-    (its query heads' dQ and the group's dK, dV) and the rest is checked for
-    finiteness."""
+def test_bwd_full_size_whole_tensor(cuda_lib):
+    """Training shape B8 H16 N2048 d128 causal: the whole dQ, dK and dV of the
+    full-size launch against the oracle, per tensor and per (batch, head)
+    plane (a plane computed wrong shows even where the tensor-wide norm would
+    dilute it)."""
+    w = WORKLOADS["train_bf16_b8_h16_n2k_causal"]
+    x = make_inputs(w)
+    dq, dk, dv = _run(x, w.causal, w.scale)
+    rq, rk, rv = oracle.attention_bwd(x["q"], x["k"], x["v"], x["dO"], w.causal, w.scale)
+    errs = [check_grad(got, ref, f"{nm}") for nm, got, ref in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv))]
+    worst = 0.0
+    for nm, got, ref in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        g = got.float().cpu().numpy()
+        for b in range(ref.shape[0]):
+            for h in range(ref.shape[1]):
+                worst = max(worst, check_grad(g[b, h], ref[b, h], f"{nm} plane ({b}, {h})"))
+    print(f"training shape: dQ/dK/dV rel {errs[0]:.2e} {errs[1]:.2e} {errs[2]:.2e}; worst plane {worst:.2e}")
+
+
+@pytest.mark.parametrize("name", ["long_bf16_b1_h16_n16k_causal", "gqa_bf16_b4_hq32_hkv8_n4k_causal", HEADLINE])
+def test_bwd_full_size_groups(cuda_lib, name):
+    """Full-size launch; the oracle checks the first, a middle and the last
+    (batch, kv-head) group entirely (its query heads' dQ and the group's dK,
+    dV) and the rest is checked for finiteness."""
     w = WORKLOADS[name]
     x = make_inputs(w)
     dq, dk, dv = _run(x, w.causal, w.scale)
-    b, g = w.B - 1, w.Hkv - 1
     G = w.Hq // w.Hkv
-    rq, rk, rv = oracle.attention_bwd_group(x["q"], x["k"], x["v"], x["dO"], b, g, w.causal, w.scale)
-    check_grad(dq[b, g * G:(g + 1) * G], rq, f"{name} dQ")
-    check_grad(dk[b, g], rk, f"{name} dK")
-    check_grad(dv[b, g], rv, f"{name} dV")
+    for b, g in ((0, 0), (w.B // 2, w.Hkv // 2), (w.B - 1, w.Hkv - 1)):
+        rq, rk, rv = oracle.attention_bwd_group(x["q"], x["k"], x["v"], x["dO"], b, g, w.causal, w.scale)
+        check_grad(dq[b, g * G:(g + 1) * G], rq, f"{name} ({b}, {g}) dQ")
+        check_grad(dk[b, g], rk, f"{name} ({b}, {g}) dK")
+        check_grad(dv[b, g], rv, f"{name} ({b}, {g}) dV")
     for t in (dq, dk, dv):
         assert torch.isfinite(t).all()

@@ -80,27 +80,45 @@ def test_fwd_large_scores_lazy_rescale(cuda_lib):
         check_lse(lse, lse_ref)
 
 
-def _sample_rows(w, n, seed):
-    g = np.random.default_rng(seed)
-    rows = [(0, 0, 0), (w.B - 1, w.Hq - 1, w.N - 1), (0, w.Hq - 1, 127), (w.B - 1, 0, 128)]
-    for _ in range(n - len(rows)):
-        rows.append((int(g.integers(w.B)), int(g.integers(w.Hq)), int(g.integers(w.N))))
-    return rows
+def _plane_rows(w):
+    """Every row of the first, a middle and the last (batch, head) plane, and
+    every row of the first and last Q tile of every plane: all CTAs of three
+    planes and the first- and last-ordered CTAs of the others."""
+    rows = set()
+    for b, h in ((0, 0), (w.B // 2, w.Hq // 2), (w.B - 1, w.Hq - 1)):
+        rows.update((b, h, r) for r in range(w.N))
+    edge = list(range(128)) + list(range(w.N - 128, w.N))
+    for b in range(w.B):
+        for h in range(w.Hq):
+            rows.update((b, h, r) for r in edge)
+    return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["train_bf16_b8_h16_n2k_causal", "long_bf16_b1_h16_n16k_causal",
-                                  "gqa_bf16_b4_hq32_hkv8_n4k_causal", HEADLINE])
-def test_fwd_full_size_sampled_rows(cuda_lib, name):
+@pytest.mark.parametrize("name", ["train_bf16_b8_h16_n2k_causal", "gqa_bf16_b4_hq32_hkv8_n4k_causal"])
+def test_fwd_full_size_whole_tensor(cuda_lib, name):
+    """Whole O and LSE of the full-size launch against the oracle, element by
+    element (the O bound is element-wise, the LSE bound max-abs)."""
     w = WORKLOADS[name]
     x = make_inputs(w, with_grad=False)
     o, lse = _run_fwd(x, w.causal, w.scale)
-    rows = _sample_rows(w, 48, 5)
+    o_ref, lse_ref = oracle.attention_fwd(x["q"], x["k"], x["v"], w.causal, w.scale)
+    err = check_o(o, o_ref, f"{name} O")
+    lerr = check_lse(lse, lse_ref, f"{name} LSE")
+    print(f"{name}: O max-abs {err:.2e}, LSE max-abs {lerr:.2e} over all {o.numel()} elements")
+
+
+@pytest.mark.parametrize("name", ["long_bf16_b1_h16_n16k_causal", HEADLINE])
+def test_fwd_full_size_planes(cuda_lib, name):
+    w = WORKLOADS[name]
+    x = make_inputs(w, with_grad=False)
+    o, lse = _run_fwd(x, w.causal, w.scale)
+    rows = _plane_rows(w)
     o_ref, lse_ref = oracle.attention_fwd_rows(x["q"], x["k"], x["v"], rows, w.causal, w.scale)
     idx = tuple(np.array(rows).T)
-    check_o(o[idx], o_ref, f"{name} O")
-    check_lse(lse[idx], lse_ref, f"{name} LSE")
-    # properties at full size: finite everywhere, LSE >= row max of a causal
-    # row's first key score, and |O| bounded by max |V| of the head
+    err = check_o(o[idx], o_ref, f"{name} O")
+    lerr = check_lse(lse[idx], lse_ref, f"{name} LSE")
+    print(f"{name}: O max-abs {err:.2e}, LSE max-abs {lerr:.2e} over {len(rows)} rows")
+    # properties at full size: finite everywhere, |O| bounded by max |V|
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
     assert o.abs().max() <= x["v"].abs().max().cuda() + 1e-2
 
