@@ -636,7 +636,23 @@ def _configs_leg(a, dev, stream, peaks, flush):
         b_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
         ftf = w.fwd_flops() / (f_ms * 1e-3) / 1e12
         btf = w.bwd_flops() / (b_ms * 1e-3) / 1e12
+        # the persistent forward (fa_fwd_persistent) on the same inputs
+        for _ in range(3):
+            _lib.fa_fwd_persistent(q, k, v, o, lse, w.causal, w.scale, stream)
+        torch.cuda.synchronize()
+        evp = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            evp[i][0].record(stream)
+            _lib.fa_fwd_persistent(q, k, v, o, lse, w.causal, w.scale, stream)
+            evp[i][1].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        if _lib.fa_get_device_status(stream) != _lib.FA_OK:
+            raise RuntimeError(f"a bounded device wait ran out during the {name} leg (persistent forward)")
+        p_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evp)
+        ptf = w.fwd_flops() / (p_ms * 1e-3) / 1e12
         leg = {"B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d, "dtype": w.dtype, "causal": w.causal,
+               "fwd_persistent_ms": round(p_ms, 4), "fwd_persistent_tflops": round(ptf, 1),
                "fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4), "fwd_tflops": round(ftf, 1),
                "bwd_tflops": round(btf, 1), "fwd_frac_of_peak": round(ftf / peaks["bf16_tflops"], 4),
                "bwd_frac_of_peak": round(btf / peaks["bf16_tflops"], 4), "launches_per_step": 4}

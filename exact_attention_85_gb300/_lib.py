@@ -21,7 +21,7 @@ EXPORTS = (
     "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_two_pass", "fa_bwd_two_pass_workspace_bytes",
     "fa_bwd_noalloc", "fa_hadamard_quant_fp8",
     "fa_hadamard_quant_workspace_bytes", "fa_fwd_fp8", "fa_get_device_status",
-    "fa_selftest_bounded_wait", "fa_status_string", "fa_fwd_f32_out", "fa_probe_exp2",
+    "fa_selftest_bounded_wait", "fa_status_string", "fa_fwd_f32_out", "fa_probe_exp2", "fa_fwd_persistent",
 )
 
 _lock = threading.Lock()
@@ -48,6 +48,7 @@ def load():
         lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_fwd_local.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_fwd_f32_out.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
+        lib.fa_fwd_persistent.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P]
         lib.fa_bwd_local.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, Z, P]
         lib.fa_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, P]
         lib.fa_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, Z, P]
@@ -70,7 +71,7 @@ def load():
         lib.fa_probe_exp2.restype = ctypes.c_longlong
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
-        for name in ("fa_fwd", "fa_fwd_local", "fa_fwd_f32_out", "fa_bwd_local", "fa_fwd_varlen", "fa_bwd_varlen",
+        for name in ("fa_fwd", "fa_fwd_local", "fa_fwd_f32_out", "fa_fwd_persistent", "fa_bwd_local", "fa_fwd_varlen", "fa_bwd_varlen",
                      "fa_bwd", "fa_bwd_two_pass", "fa_bwd_noalloc", "fa_hadamard_quant_fp8", "fa_fwd_fp8",
                      "fa_get_device_status", "fa_selftest_bounded_wait"):
             getattr(lib, name).restype = I
@@ -115,6 +116,14 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None):
     B, Hq, Hkv, N, d = _dims(q, k)
     _check("fa_fwd", load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
                                    int(causal), float(scale), _dtype_code(q), _stream(stream)))
+
+
+def fa_fwd_persistent(q, k, v, o, lse, causal: bool, scale: float, stream=None):
+    """fa_fwd as the persistent kernel (dynamic block schedule); same results."""
+    B, Hq, Hkv, N, d = _dims(q, k)
+    _check("fa_fwd_persistent", load().fa_fwd_persistent(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq,
+                                                         Hkv, N, d, int(causal), float(scale), _dtype_code(q),
+                                                         _stream(stream)))
 
 
 def fa_fwd_f32_out(q, k, v, o_f32, lse, causal: bool, scale: float, stream=None):

@@ -28,9 +28,10 @@ struct FaRange {
 
 namespace fa {
 
-// One status word per device that loads the library (module-scope device
-// variable); kernels receive its address as a parameter.
-__device__ unsigned int g_status_word;
+// Two status words per device that loads the library (module-scope device
+// variable, status.cuh): timeouts, then the other conditions.  Kernels
+// receive the address of the first as a parameter.
+__device__ unsigned int g_status_word[2];
 
 namespace {
 
@@ -174,7 +175,7 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 // Shared validation and launch of the forward entry points (window 0: none).
 fa_status_t fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
                        int N, int d, int causal, int window, float scale, fa_dtype_t dtype, void *stream,
-                       const fa::SeqLayout *packed = nullptr, bool o_f32 = false) {
+                       const fa::SeqLayout *packed = nullptr, bool o_f32 = false, bool persistent = false) {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return FA_ERR_INVALID_ARG;
@@ -184,6 +185,7 @@ fa_status_t fwd_common(const void *q, const void *k, const void *v, void *o, flo
     fa::SeqLayout lay{0, B, N, B * N, nullptr};
     if (packed) lay = *packed;
     fa::FwdArgs a{q, k, v, o, lse, B, Hq, Hkv, N, d, causal, scale, dtype == FA_BF16, window, lay, o_f32};
+    if (persistent) return from_cuda(fa::launch_fwd_persist(a, static_cast<cudaStream_t>(stream)));
     return from_cuda(fa::launch_fwd(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -236,6 +238,13 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
                    int N, int d, int causal, float scale, fa_dtype_t dtype, void *stream) {
     FA_RANGE("fa_fwd");
     return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, stream);
+}
+
+fa_status_t fa_fwd_persistent(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+                              int Hkv, int N, int d, int causal, float scale, fa_dtype_t dtype, void *stream) {
+    FA_RANGE("fa_fwd_persistent");
+    return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, stream, nullptr, false,
+                      true);
 }
 
 fa_status_t fa_fwd_f32_out(const void *q, const void *k, const void *v, float *o_f32, float *lse, int B, int Hq,
@@ -372,13 +381,13 @@ fa_status_t fa_get_device_status(void *stream) {
     unsigned int *p = fa::device_status_ptr();
     if (!p) return FA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    unsigned int host = 0;
-    if (cudaMemcpyAsync(&host, p, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess) return FA_ERR_CUDA;
-    if (cudaMemsetAsync(p, 0, sizeof(unsigned int), st) != cudaSuccess) return FA_ERR_CUDA;
+    unsigned int host[2] = {0u, 0u};
+    if (cudaMemcpyAsync(host, p, sizeof(host), cudaMemcpyDeviceToHost, st) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemsetAsync(p, 0, sizeof(host), st) != cudaSuccess) return FA_ERR_CUDA;
     if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
-    if (host & fa::kStatusTimeout) return FA_ERR_TIMEOUT;
-    if (host & fa::kStatusBadLaunch) return FA_ERR_CUDA;
-    return (host & fa::kStatusBadArgs) ? FA_ERR_INVALID_ARG : FA_OK;
+    if (host[0] & fa::kStatusTimeout) return FA_ERR_TIMEOUT;
+    if (host[1] & fa::kStatusBadLaunch) return FA_ERR_CUDA;
+    return (host[1] & fa::kStatusBadArgs) ? FA_ERR_INVALID_ARG : FA_OK;
 }
 
 long long fa_probe_exp2(float *sink, int blocks, int iters, void *stream) {

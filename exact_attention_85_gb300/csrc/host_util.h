@@ -40,7 +40,7 @@ bool make_tmap_3d_box(CUtensorMap *map, const void *base, CUtensorMapDataType dt
 bool make_tmap_tiles(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, int d, const SeqLayout &lay,
                      int heads, uint32_t rows);
 
-// Device address of this library's status word on the current device
+// Device address of this library's status words (status.cuh) on the current device
 // (looked up once per device and context, cached).
 unsigned int *device_status_ptr();
 
@@ -95,6 +95,8 @@ struct QuantArgs {
 };
 
 cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st);
+// The persistent forward (dense layout, no window, 16-bit output only).
+cudaError_t launch_fwd_persist(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool two_pass);
 cudaError_t launch_fwd_fp8(const Fp8FwdArgs &a, cudaStream_t st);
 cudaError_t launch_hadamard_quant(const QuantArgs &a, cudaStream_t st);

@@ -26,7 +26,7 @@
  *           (FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_WORKSPACE) and
  *           leave every output untouched.  A failed launch returns
  *           FA_ERR_CUDA.  Device-side waits are bounded: a wait that runs out
- *           records FA_ERR_TIMEOUT in a per-device status word (read it with
+ *           records FA_ERR_TIMEOUT in a per-device status (read it with
  *           fa_get_device_status) and the kernel returns instead of hanging.
  * Scores.   S = scale * Q K^T; causal masking is top-left aligned (query row r
  *           sees key c iff c <= r).  LSE is the natural-log log-sum-exp of the
@@ -66,6 +66,25 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
 fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
                    float *lse, int B, int Hq, int Hkv, int N, int d,
                    int causal, float scale, fa_dtype_t dtype, void *stream);
+
+/*
+ * The forward of fa_fwd as a persistent kernel with a dynamic block schedule.
+ * [FA3] "remaining optimisations" (persistent kernel); the arithmetic is
+ * fa_fwd's ([V2] section 6.1, [CSDN] 3.1.1), and for the same arguments O and
+ * LSE are bit-identical to fa_fwd's.  The grid holds one CTA per 256-row
+ * block in fa_fwd's longest-first order, but every CTA that runs keeps
+ * running: it cancels CTAs that have not been launched yet (cluster launch
+ * control) and works on their blocks, so blocks are handed out dynamically
+ * with no counter in global memory, and each block's loads, first MMAs and
+ * epilogue overlap the neighbouring block's work.  It pays off where blocks
+ * are short (short sequences); fa_fwd itself uses it for the shapes where it
+ * was measured faster.
+ *   Arguments, layouts and errors exactly as fa_fwd.
+ */
+fa_status_t fa_fwd_persistent(const void *q, const void *k, const void *v,
+                              void *o, float *lse, int B, int Hq, int Hkv,
+                              int N, int d, int causal, float scale,
+                              fa_dtype_t dtype, void *stream);
 
 /*
  * Debug forward: fa_fwd with O written in fp32, i.e. O~ / l before any
@@ -306,20 +325,20 @@ fa_status_t fa_fwd_fp8(const void *q8, const void *k8, const void *v8,
                        float scale, void *stream);
 
 /*
- * Reads and clears the current device's status word, which kernels set when
+ * Reads and clears the current device's status, which kernels set when
  * a bounded wait runs out, when packed sequence offsets read on the device
  * break the rules of fa_fwd_varlen, or when a kernel finds its shared-memory
  * window misaligned for its tiles (it then does nothing).  Synchronises
  * `stream` first.  Returns, in this order of precedence: FA_ERR_TIMEOUT (a
  * wait ran out), FA_ERR_CUDA (a kernel could not use its launch
- * configuration, or the copy of the word itself failed), FA_ERR_INVALID_ARG
+ * configuration, or the copy of the status itself failed), FA_ERR_INVALID_ARG
  * (bad device-side offsets), else FA_OK.
- *   There is ONE status word per device, shared by every caller, thread and
+ *   There is ONE status per device, shared by every caller, thread and
  *   stream of the process, and this call clears it for all of them.  With
  *   several streams or callers in flight, a status read on one stream may
  *   report a condition raised by work on another (and that other caller's
  *   later read then sees FA_OK).  Callers that need to attribute a failure
- *   must serialise their work and their reads of the status word.
+ *   must serialise their work and their reads of the status.
  */
 fa_status_t fa_get_device_status(void *stream);
 
@@ -342,7 +361,7 @@ long long fa_probe_exp2(float *sink, int blocks, int iters, void *stream);
  * Self-test of the bounded-wait machinery: launches one block that waits on a
  * barrier nothing will ever complete, with a limit of `timeout_us`
  * microseconds (1 .. 1000000).  The wait runs out, the kernel records
- * FA_ERR_TIMEOUT in the status word and returns; nothing faults or hangs.
+ * FA_ERR_TIMEOUT in the device status and returns; nothing faults or hangs.
  */
 fa_status_t fa_selftest_bounded_wait(int timeout_us, void *stream);
 

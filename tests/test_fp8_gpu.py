@@ -75,8 +75,8 @@ def _rel_rms(got, ref):
 def _rms_vs_v(got, ref, v):
     """RMS error of O relative to the RMS of the values V."""
     g = got.float().cpu().numpy().astype(np.float64) if hasattr(got, "cpu") else got
-    vv = v.double().numpy() if hasattr(v, "numpy") else v
-    return float(np.sqrt(np.mean((g - ref) ** 2)) / np.sqrt(np.mean(vv ** 2)))
+    v_rms = float(v.float().pow(2).mean().sqrt()) if hasattr(v, "float") else float(np.sqrt(np.mean(v ** 2)))
+    return float(np.sqrt(np.mean((g - ref) ** 2)) / v_rms)
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,N,causal", [(1, 2, 2, 300, False), (2, 4, 2, 513, True), (1, 1, 1, 128, False)])
@@ -138,8 +138,10 @@ def test_fp8_outlier_workload_full_size(cuda_lib):
         assert dev <= FP8_REL_RMS
     e_had = _rel_rms(got["hadamard"], o_ref)
     e_plain = _rel_rms(got["plain"], o_ref)
-    v_rows = x["v"][idx[0], idx[1] // (w.Hq // w.Hkv)]  # V of each row's head
+    # printed only: the error relative to the RMS of all of V (every head of
+    # V is drawn from the same distribution)
     print(f"fp8 outliers vs exact attention (relative RMS, bound 0.03 not met by e4m3 inputs): "
           f"hadamard {e_had:.4f}, plain {e_plain:.4f}, ratio {e_plain / e_had:.2f}; RMS error / RMS(V): "
-          f"hadamard {_rms_vs_v(got['hadamard'], o_ref, v_rows):.4f}, plain {_rms_vs_v(got['plain'], o_ref, v_rows):.4f}")
+          f"hadamard {_rms_vs_v(got['hadamard'], o_ref, x['v']):.4f}, "
+          f"plain {_rms_vs_v(got['plain'], o_ref, x['v']):.4f}")
     assert e_had <= e_plain
