@@ -35,6 +35,10 @@ SHAPES = [
     (1, 4, 1, 1000, 64, torch.bfloat16, True),
     (1, 2, 2, 640, 128, torch.float16, True),
     (3, 2, 2, 256, 64, torch.bfloat16, False),
+    # beyond the persistent kernel's range (fa_fwd runs the one-CTA-per-block
+    # kernel): ragged tails there too
+    (1, 2, 1, 2300, 128, torch.bfloat16, True),
+    (1, 2, 2, 1100, 64, torch.float16, False),
 ]
 
 
