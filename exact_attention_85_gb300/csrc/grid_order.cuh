@@ -14,15 +14,17 @@
 
 namespace fa {
 
-// Group size for `blocks` blocks per plane on `sms` SMs: a group's work on
-// all SMs must last longer than one plane's longest block (about 2 / blocks
-// of a plane's causal work), with a margin of 1.5.  The planes are then
+// Group size for `blocks` blocks per plane on `sms` SMs: about four waves
+// of blocks per group, so that a group's work on all SMs lasts well beyond
+// one plane's longest block (about 2 / blocks of a plane's causal work);
+// measured against three waves: headline forward +2.7 %, backward +1 %,
+// long-sequence backward +1 %, training-shape backward -1.5 %.  The planes are then
 // spread evenly over the groups that size implies: a small last group would
 // start its planes' longest blocks near the end of the grid, where nothing
 // is left to overlap them (with 32 planes, groups of 15, 15 and 2 left the
 // SMs idle for a sixth of a grouped-query backward; 11, 11 and 10 do not).
 inline int grid_group_planes(int planes, int blocks, int sms) {
-    int g = (3 * sms + blocks - 1) / (blocks > 0 ? blocks : 1);
+    int g = (4 * sms + blocks - 1) / (blocks > 0 ? blocks : 1);
     if (g < 1) g = 1;
     if (g > planes) g = planes;
     const int ngroups = (planes + g - 1) / g;
