@@ -596,11 +596,12 @@ cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st) {
     // Short sequences go to the persistent kernel (fa_fwd_persist.cu, same
     // results bit for bit): with few K/V tiles per 256-row block, the set-up
     // and epilogue it overlaps across blocks weigh most.  Crossover measured
-    // on a GB300 (bf16, d = 128, 16 heads): causal N = 512 / 1024 / 2048 ran
-    // 1.26x / 1.10-1.14x / 1.01-1.02x faster, N = 3072 / 4096 0.94x / 0.97x;
-    // without the mask N = 1024 1.03x, N = 2048 0.99x, N = 4096 0.97x.
+    // on a GB300 (bf16, d = 128, 16 heads, L2 flushed): causal N = 512 / 1024
+    // / 2048 ran 1.3x / 1.1x / 1.01-1.03x faster than one CTA per block,
+    // N = 3072 / 4096 / 8192 0.99x / 0.98x / 0.97x; without the mask
+    // N = 1024 1.08x, N = 2048 1.02x, N = 4096 0.97x.
     const bool dense = a.window == 0 && !a.lay.varlen && !a.o_f32;
-    if (dense && (a.causal ? a.N <= 2048 : a.N <= 1024)) return launch_fwd_persist(a, st);
+    if (dense && a.N <= 2048) return launch_fwd_persist(a, st);
     if (a.d == 128) return a.bf16 ? launch_fwd_t<128, true>(a, st) : launch_fwd_t<128, false>(a, st);
     if (a.d == 64) return a.bf16 ? launch_fwd_t<64, true>(a, st) : launch_fwd_t<64, false>(a, st);
     return cudaErrorInvalidValue;

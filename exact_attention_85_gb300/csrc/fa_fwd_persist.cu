@@ -22,8 +22,9 @@
 // block's S_A(0) and S_B(0) are issued right after the current block's last
 // P.V MMAs, and each softmax warpgroup's epilogue (O = O~ / l, L = m + ln l)
 // runs while the tensor cores work on the other tile and on the next block.
-// O rows are stored by their own threads (the Q buffer that stages O in the
-// plain forward is already being refilled).
+// O rows are stored by their own threads, one whole 32-byte sector per store
+// (the Q buffer that stages O in the plain forward is already being
+// refilled).
 //
 // Per block the arithmetic is that of fa_fwd.cu (two 128-row Q tiles A and B
 // walking the same K/V stream, ping-ponged softmax warpgroups, exact lazy
@@ -511,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv_l = 1.0f / l_sum;
             const bool in = q0 + row < p.N;
             const size_t r = (size_t)blk.bh * p.N + q0 + row;
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.o) + r * (D * 2));
+            uint8_t *dst = static_cast<uint8_t *>(p.o) + r * (D * 2);
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
@@ -524,9 +525,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float a1 = __uint_as_float(o[2 * c + 1]) * inv_l;
                     w[c] = BF16 ? pack_bf16x2(a0, a1) : pack_f16x2(a0, a1);
                 }
-                if (in) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) dst[c0 / 8 + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                if (in) {  // 64 bytes of the row: two whole 32-byte sectors
+                    st_global_v8(dst + c0 * 2, w);
+                    st_global_v8(dst + c0 * 2 + 32, w + 8);
                 }
             }
             if (in) p.lse[r] = (m_ref + log2f(l_exact)) * 0.69314718055994530942f;

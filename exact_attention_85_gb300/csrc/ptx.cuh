@@ -333,6 +333,13 @@ __device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t *r) {
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 32-byte global store (sm_100+): one whole 32-byte sector per thread, so a
+// row written thread by thread reaches L2 as full sectors.  `p` must be
+// 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *r) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), FA_I8(0) : "memory");
+}
+
 // ------------------------------------------------------------ arithmetic
 
 __device__ __forceinline__ float ex2_approx(float x) {

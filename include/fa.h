@@ -62,9 +62,8 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
  *   q [B][Hq][N][d], k, v [B][Hkv][N][d]  (in, element type `dtype`)
  *   o [B][Hq][N][d]                       (out, element type `dtype`)
  *   lse [B][Hq][N]                        (out, fp32, natural log)
- * Short sequences (causal N <= 2048, non-causal N <= 1024) run the kernel of
- * fa_fwd_persistent, longer ones one CTA per 256-row block; both give the
- * same bits.
+ * Short sequences (N <= 2048) run the kernel of fa_fwd_persistent, longer
+ * ones one CTA per 256-row block; both give the same bits.
  */
 fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
                    float *lse, int B, int Hq, int Hkv, int N, int d,
