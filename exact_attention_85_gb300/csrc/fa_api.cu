@@ -243,6 +243,7 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o, float *
 fa_status_t fa_fwd_persistent(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
                               int Hkv, int N, int d, int causal, float scale, fa_dtype_t dtype, void *stream) {
     FA_RANGE("fa_fwd_persistent");
+    if (reinterpret_cast<uintptr_t>(o) & 31u) return FA_ERR_INVALID_ARG;  // O rows are stored 32 bytes at a time
     return fwd_common(q, k, v, o, lse, B, Hq, Hkv, N, d, causal ? 1 : 0, 0, scale, dtype, stream, nullptr, false,
                       true);
 }

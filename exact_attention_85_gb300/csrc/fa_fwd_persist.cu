@@ -580,6 +580,7 @@ cudaError_t launch_fwd_persist_t(const FwdArgs &a, cudaStream_t st) {
 
 cudaError_t launch_fwd_persist(const FwdArgs &a, cudaStream_t st) {
     if (a.window > 0 || a.lay.varlen || a.o_f32) return cudaErrorInvalidValue;  // dense, 16-bit output only
+    if (reinterpret_cast<uintptr_t>(a.o) & 31u) return cudaErrorInvalidValue;     // 32-byte row stores
     if (a.d == 128) return a.bf16 ? launch_fwd_persist_t<128, true>(a, st) : launch_fwd_persist_t<128, false>(a, st);
     if (a.d == 64) return a.bf16 ? launch_fwd_persist_t<64, true>(a, st) : launch_fwd_persist_t<64, false>(a, st);
     return cudaErrorInvalidValue;

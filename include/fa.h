@@ -81,7 +81,10 @@ fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
  * epilogue overlap the neighbouring block's work.  It pays off where blocks
  * are short (short sequences); fa_fwd itself uses it for the shapes where it
  * was measured faster.
- *   Arguments, layouts and errors exactly as fa_fwd.
+ *   Arguments, layouts and errors as fa_fwd, except that o must be 32-byte
+ *   aligned (its rows are stored 32 bytes at a time; FA_ERR_INVALID_ARG
+ *   otherwise).  fa_fwd falls back to the one-CTA-per-block kernel when o is
+ *   only 16-byte aligned.
  */
 fa_status_t fa_fwd_persistent(const void *q, const void *k, const void *v,
                               void *o, float *lse, int B, int Hq, int Hkv,

@@ -66,6 +66,21 @@ def test_fwd_argument_validation(lib):
     assert _fwd(lib, B=1 << 12, Hq=1 << 10, Hkv=1, N=1 << 12) == 2  # too many elements
 
 
+def test_persistent_forward_needs_32_byte_aligned_output(lib):
+    """fa_fwd_persistent stores O rows 32 bytes at a time: an O that is only
+    16-byte aligned is refused before anything is launched (fa_fwd itself
+    falls back to the one-CTA-per-block kernel for it); the other checks are
+    fa_fwd's."""
+    def pers(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, Hq=2, Hkv=1, N=16, d=128, causal=0, scale=0.1,
+                 dtype=1)
+        a.update(kw)
+        return lib.fa_fwd_persistent(*a.values(), None)
+    assert pers(o=FAKE + 16) == 1
+    assert pers(q=None) == 1
+    assert pers(d=96) == 2
+
+
 def test_bwd_argument_validation(lib):
     ws_need = lib.fa_bwd_workspace_bytes(1, 2, 16, 128)
     assert ws_need == 256 + 2 * 16 * 128 * 4

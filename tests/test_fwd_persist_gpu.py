@@ -110,3 +110,24 @@ def test_persistent_full_size_bit_identical_to_plain(cuda_lib, name):
     idx = tuple(np.array(rows).T)
     check_o(o[idx], o_ref, f"{name} O")
     check_lse(lse[idx], lse_ref, f"{name} LSE")
+
+
+def test_fwd_with_16_byte_aligned_output_falls_back(cuda_lib):
+    """fa_fwd at a short sequence length with O only 16-byte aligned: the
+    persistent kernel (32-byte row stores) is skipped for the one-CTA-per-block
+    kernel, and the result still matches the oracle."""
+    B, Hq, N, d = 2, 4, 700, 128
+    x = make_custom(B, Hq, Hq, N, d, torch.bfloat16, seed=29, with_grad=False)
+    q, k, v = (x[n].cuda().contiguous() for n in ("q", "k", "v"))
+    buf = torch.empty(B * Hq * N * d + 8, dtype=torch.bfloat16, device="cuda")
+    o = buf[8:].view(B, Hq, N, d)  # 16 bytes past a 32-byte boundary
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+    _lib.fa_fwd(q, k, v, o, lse, True, d ** -0.5)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    o_ref, lse_ref = oracle.attention_fwd(x["q"], x["k"], x["v"], True, d ** -0.5)
+    check_o(o, o_ref)
+    check_lse(lse, lse_ref)
+    with pytest.raises(_lib.FAError):
+        _lib.fa_fwd_persistent(q, k, v, o, lse, True, d ** -0.5)
