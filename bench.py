@@ -241,10 +241,10 @@ def run_ours(a):
     # roofline of the dominant kernel (the longer of the two timed calls)
     if has_bwd and bwd_avg > fwd_avg:
         dom, dom_ms, dom_flops = "fa_bwd (main kernel; duration includes the small D and dQ-convert kernels)", bwd_avg, f_bwd
-        traffic = _traffic("bwd_kernel", ["fa_bwd.cu"])
+        traffic = _traffic("bwd_kernel", ["fa_bwd.cu", "grid_order.cuh"])
     else:
         dom, dom_ms, dom_flops = "fwd_kernel", fwd_avg, f_fwd
-        traffic = _traffic("fwd_kernel", ["fa_fwd.cu"])
+        traffic = _traffic("fwd_kernel", ["fa_fwd.cu", "grid_order.cuh"])
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": traffic,
