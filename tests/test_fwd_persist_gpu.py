@@ -131,3 +131,27 @@ def test_fwd_with_16_byte_aligned_output_falls_back(cuda_lib):
     check_lse(lse, lse_ref)
     with pytest.raises(_lib.FAError):
         _lib.fa_fwd_persistent(q, k, v, o, lse, True, d ** -0.5)
+
+
+def test_persistent_concurrent_streams(cuda_lib):
+    """Two persistent forwards with different inputs running at the same time
+    on two streams: each grid takes only its own not-yet-launched CTAs' blocks
+    (a cancelled CTA belongs to the grid that cancelled it), so both results
+    match their oracle and their one-stream runs bit for bit."""
+    d = 128
+    xs = [make_custom(16, 8, 8, 1024, d, torch.bfloat16, seed=s, with_grad=False) for s in (41, 42)]
+    dev = [{n: x[n].cuda().contiguous() for n in ("q", "k", "v")} for x in xs]
+    outs = [(torch.empty_like(t["q"]), torch.empty((16, 8, 1024), dtype=torch.float32, device="cuda")) for t in dev]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for t, (o, lse), st in zip(dev, outs, streams):
+            _lib.fa_fwd_persistent(t["q"], t["k"], t["v"], o, lse, True, d ** -0.5, st)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    for x, t, (o, lse) in zip(xs, dev, outs):
+        alone_o, alone_lse = _run(x, True, d ** -0.5)
+        assert torch.equal(o, alone_o) and torch.equal(lse, alone_lse)
+    o_ref, lse_ref = oracle.attention_fwd(xs[1]["q"], xs[1]["k"], xs[1]["v"], True, d ** -0.5)
+    check_o(outs[1][0], o_ref)
+    check_lse(outs[1][1], lse_ref)
