@@ -98,6 +98,10 @@ cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st);
 // The persistent forward (dense layout, no window, 16-bit output only).
 cudaError_t launch_fwd_persist(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_bwd(const BwdArgs &a, cudaStream_t st, bool two_pass);
+// The persistent main kernel of the backward (dense layout, atomic dQ, dK and
+// dV 32-byte aligned): the step between fa_bwd's D preprocessing and its dQ
+// conversion.
+cudaError_t launch_bwd_persist_main(const BwdArgs &a, cudaStream_t st);
 cudaError_t launch_fwd_fp8(const Fp8FwdArgs &a, cudaStream_t st);
 cudaError_t launch_hadamard_quant(const QuantArgs &a, cudaStream_t st);
 cudaError_t launch_selftest_wait(int timeout_us, cudaStream_t st);

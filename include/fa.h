@@ -146,6 +146,10 @@ size_t fa_bwd_workspace_bytes(int B, int Hq, int N, int d);
  *   bytes, 256-byte aligned; its contents on entry do not matter.
  * dQ is accumulated with fp32 atomic reductions, so it is deterministic only
  * up to the order of those additions.
+ * Short sequences (N <= 1024, with dK and dV 32-byte aligned) run a
+ * persistent main kernel (work items handed out by cluster launch control,
+ * as in fa_fwd_persistent); dK and dV are the same bits either way, dQ the
+ * same up to the order of its fp32 atomic additions.
  */
 fa_status_t fa_bwd(const void *q, const void *k, const void *v, const void *o,
                    const float *lse, const void *dO, void *dq, void *dk,
