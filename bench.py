@@ -13,10 +13,12 @@ Besides the contract keys the line carries, for the headline shape:
 throughput probe and the exp-bound time of each direction),
 ``two_pass_bwd_leg``, ``window_leg``, ``varlen_leg`` and ``fp8_leg`` (the
 deterministic backward, sliding window, packed batch and FP8 rows on their
-own workloads), and ``configs_leg`` (forward and backward of the tiny fp16,
-training, long-context and grouped-query workloads; the fp64 oracle's host
-time on a bounded sample of each is in ``cpu_baseline.per_workload``); each
-can be switched off with its ``--no-*`` flag.
+own workloads), ``short_seq_leg`` (causal N = 512 and 1024, where both
+directions run their persistent kernels), and ``configs_leg`` (forward and
+backward of the tiny fp16, training, long-context and grouped-query
+workloads; the fp64 oracle's host time on a bounded sample of each is in
+``cpu_baseline.per_workload``); each can be switched off with its ``--no-*``
+flag (``--no-configs`` covers the short-sequence leg too).
 
 ``--impl reference`` times the fp64 CPU oracle (test infrastructure, the
 only other place this script runs it) on a bounded sample of the same
@@ -283,6 +285,7 @@ def run_ours(a):
         result["fp8_leg"] = _fp8_leg(a, dev, stream, peaks)
     if not a.no_configs and a.workload is None:
         result["configs_leg"] = _configs_leg(a, dev, stream, peaks, flush)
+        result["short_seq_leg"] = _short_leg(a, dev, stream, peaks, flush)
     if not a.no_e2e:
         result["e2e"] = _e2e(a, w, host, dev, stream, has_bwd, ws)
     if rank == 0 and ws == 1 and not a.no_cpu:
@@ -586,6 +589,9 @@ def _fp8_leg(a, dev, stream, peaks):
 
 CONFIG_LEGS = ("tiny_fp16_d64_n256", "train_bf16_b8_h16_n2k_causal", "long_bf16_b1_h16_n16k_causal",
                "gqa_bf16_b4_hq32_hkv8_n4k_causal")
+# short sequences (bf16, d = 128, 16 heads, causal), where fa_fwd and fa_bwd
+# run their persistent kernels: (B, N)
+SHORT_LEGS = ((32, 512), (16, 1024))
 
 
 def _configs_leg(a, dev, stream, peaks, flush):
@@ -657,6 +663,54 @@ def _configs_leg(a, dev, stream, peaks, flush):
                "bwd_tflops": round(btf, 1), "fwd_frac_of_peak": round(ftf / peaks["bf16_tflops"], 4),
                "bwd_frac_of_peak": round(btf / peaks["bf16_tflops"], 4), "launches_per_step": 4}
         out[name] = leg
+        del q, k, v, dO, o, lse, dq, dk, dv, wsb
+    return out
+
+
+def _short_leg(a, dev, stream, peaks, flush):
+    """fa_fwd / fa_bwd at short causal lengths (SHORT_LEGS), where both run
+    their persistent kernels, timed like the step (L2 flushed between
+    steps)."""
+    import torch
+
+    from exact_attention_85_gb300 import _lib
+    from exact_attention_85_gb300.inputs import make_custom
+
+    out = {}
+    for B, N in SHORT_LEGS:
+        H, d = 16, 128
+        x = make_custom(B, H, H, N, d, torch.bfloat16, seed=N)
+        q, k, v, dO = (x[n].to(dev).contiguous() for n in ("q", "k", "v", "dO"))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsb = torch.empty(_lib.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+        scale = d ** -0.5
+        for _ in range(max(3, a.warmup)):
+            _lib.fa_fwd(q, k, v, o, lse, True, scale, stream)
+            _lib.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, True, scale, wsb, stream)
+        torch.cuda.synchronize()
+        steps = max(3, min(a.steps, 20))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for i in range(steps):
+            ev[i][0].record(stream)
+            _lib.fa_fwd(q, k, v, o, lse, True, scale, stream)
+            ev[i][1].record(stream)
+            _lib.fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, True, scale, wsb, stream)
+            ev[i][2].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize()
+        if _lib.fa_get_device_status(stream) != _lib.FA_OK:
+            raise RuntimeError(f"a bounded device wait ran out during the short-sequence leg (N={N})")
+        f_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        b_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        f_fl = 2.0 * B * H * N * N * d
+        out[f"bf16_b{B}_h{H}_n{N}_causal"] = {
+            "fwd_ms": round(f_ms, 4), "bwd_ms": round(b_ms, 4),
+            "fwd_tflops": round(f_fl / (f_ms * 1e-3) / 1e12, 1), "bwd_tflops": round(2.5 * f_fl / (b_ms * 1e-3) / 1e12, 1),
+            "fwd_frac_of_peak": round(f_fl / (f_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "bwd_frac_of_peak": round(2.5 * f_fl / (b_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "kernels": "persistent forward and persistent backward main kernel", "launches_per_step": 4}
         del q, k, v, dO, o, lse, dq, dk, dv, wsb
     return out
 
