@@ -600,11 +600,15 @@ cudaError_t launch_fwd(const FwdArgs &a, cudaStream_t st) {
     // / 2048 ran 1.3x / 1.1x / 1.01-1.03x faster than one CTA per block,
     // N = 3072 / 4096 / 8192 0.99x / 0.98x / 0.97x; without the mask
     // N = 1024 1.08x, N = 2048 1.02x, N = 4096 0.97x.
+    // The same holds for a sliding window (a block walks at most about
+    // W / 128 + 2 K/V tiles whatever N is) and for packed batches: at
+    // N = 8192, W = 256 / 1024 / 4096 ran 1.10x / 1.05x / 0.96x; a packed
+    // batch of lengths up to 2048 1.01x, up to 7506 0.96x.
     // It stores O rows in 32-byte pieces, so it needs O 32-byte aligned (the
     // entry points promise only 16).
-    const bool dense = a.window == 0 && !a.lay.varlen && !a.o_f32;
     const bool o32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
-    if (dense && o32 && a.N <= 2048) return launch_fwd_persist(a, st);
+    const int walk = a.window > 0 ? (a.window < a.N ? a.window : a.N) : a.N;  // keys a block's rows see
+    if (!a.o_f32 && o32 && walk <= 2048) return launch_fwd_persist(a, st);
     if (a.d == 128) return a.bf16 ? launch_fwd_t<128, true>(a, st) : launch_fwd_t<128, false>(a, st);
     if (a.d == 64) return a.bf16 ? launch_fwd_t<64, true>(a, st) : launch_fwd_t<64, false>(a, st);
     return cudaErrorInvalidValue;

@@ -1,6 +1,6 @@
 // fa_fwd_persist.cu -- persistent FlashAttention-2 forward for sm_103a with a
-// dynamic, longest-first block schedule (dense layout, bf16 / fp16, d = 64 or
-// 128, causal or not, 16-bit output).
+// dynamic, longest-first block schedule (dense or packed layout, causal, full
+// or causal sliding-window mask, bf16 / fp16, d = 64 or 128, 16-bit output).
 //
 // The FlashAttention-3 summary page ("remaining optimisations": persistent
 // kernel) names a persistent kernel as the way to keep the tensor cores busy
@@ -30,6 +30,12 @@
 // walking the same K/V stream, ping-ponged softmax warpgroups, exact lazy
 // rescale by more than 8 in log2 units, P in 16 bits from tensor memory): the
 // outputs are bit-identical to the plain forward's.
+// GENERAL instances add the causal sliding window (a block's K/V stream starts
+// at the tile holding its first row's oldest visible key) and packed
+// variable-length batches (token-major rows from cu_seqlens; blocks past a
+// sequence's end are empty items, taken and dropped like any other), the two
+// cases of the FlashAttention-3 summary's GQA / sliding-window and
+// variable-length discussions whose blocks walk few K/V tiles whatever N is.
 // Warps: 0-3 softmax + epilogue of tile A, 4-7 of tile B, 8 TMA producer and
 // scheduler, 9 MMA issuer (owns the tensor memory).
 #include "grid_order.cuh"
@@ -62,8 +68,9 @@ struct PersistLayout {
     // s_full[2], p_full[2], o_final[2], item_full[2], item_empty[2], clc, drain
     static constexpr int NBAR = 2 + 2 + 2 * KS + 2 * VS + 2 + 2 + 2 + 2 + 2 + 1 + 1;
     static constexpr int OFF_CLC = OFF_BAR + NBAR * 8;   // 16-byte cancellation response
-    static constexpr int OFF_MISC = OFF_CLC + 16;        // item slots [2], TMEM base, abort flag
-    static constexpr int BYTES = OFF_MISC + 16;
+    // item slots [2] of {item, first row, rows} (16 bytes each), TMEM base, abort flag
+    static constexpr int OFF_MISC = OFF_CLC + 16;
+    static constexpr int BYTES = OFF_MISC + 48;
     static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024
     static_assert(OFF_CLC % 16 == 0, "response alignment");
     static_assert(ALLOC <= 227 * 1024, "shared memory");
@@ -73,8 +80,11 @@ struct PersistParams {
     void *o;
     float *lse;
     unsigned int *status;
-    int Hq, Hkv, N, nblk, causal;
-    int group, planes;  // CTA order (grid_order.cuh)
+    const int *cu_seqlens;  // packed batches: [B + 1] row offsets
+    int varlen, total;      // packed layout; its total rows
+    int window;             // 0: none, else a causal window of that many keys
+    int Hq, Hkv, N, nblk, causal;  // N: rows per sequence (packed: the maximum)
+    int group, planes;             // CTA order (grid_order.cuh)
     float scale_log2;
 };
 
@@ -108,25 +118,42 @@ __device__ __forceinline__ int clc_result(const void *resp) {
     return canceled ? (int)x : -1;
 }
 
-// The block an item index stands for (the plain forward's grid order).
+// The block an item index stands for (the plain forward's grid order), in a
+// sequence of n rows starting at token row0 (dense: row0 = 0, n = N).  Tile x
+// walks K/V tiles jx0 .. nx - 1 (none if nx = 0); the block's K/V stream is
+// tiles jA0 .. nmax - 1 (jB0 >= jA0, nB >= nA whenever tile B has work).
 struct Block {
-    int bh, q0a, nA, nB, nmax;
+    int bh, q0a, jA0, jB0, nA, nB, nmax, row0, n;
 };
 
-__device__ __forceinline__ Block decode_block(int item, const PersistParams &p) {
+__device__ __forceinline__ Block decode_block(int item, int row0, int n, const PersistParams &p) {
     Block blk;
     int t_lin;
     grid_decode(item, p.planes, p.nblk, p.group, blk.bh, t_lin);
     const int t = p.causal ? (p.nblk - 1 - t_lin) : t_lin;
     blk.q0a = t * 2 * kBM;
-    const int nkv_all = (p.N + kBN - 1) / kBN;
+    blk.row0 = row0;
+    blk.n = n;
+    blk.jA0 = blk.jB0 = 0;
+    if (blk.q0a >= n) {  // past the end of a shorter packed sequence: no work
+        blk.nA = blk.nB = blk.nmax = 0;
+        return blk;
+    }
+    const int nkv_all = (n + kBN - 1) / kBN;
     blk.nA = p.causal ? min(blk.q0a / kBN + 1, nkv_all) : nkv_all;
-    blk.nB = blk.q0a + kBM >= p.N ? 0 : (p.causal ? min((blk.q0a + kBM) / kBN + 1, nkv_all) : nkv_all);
+    blk.nB = blk.q0a + kBM >= n ? 0 : (p.causal ? min((blk.q0a + kBM) / kBN + 1, nkv_all) : nkv_all);
     blk.nmax = max(blk.nA, blk.nB);
+    if (p.window > 0) {
+        // row r sees keys r - W + 1 .. r: tile x starts at the tile holding
+        // key q0_x - W + 1 (the tiles before it are skipped like those above
+        // the causal diagonal)
+        blk.jA0 = max(0, blk.q0a - p.window + 1) / kBN;
+        blk.jB0 = max(0, blk.q0a + kBM - p.window + 1) / kBN;
+    }
     return blk;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool GENERAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_persist_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PersistParams p) {
@@ -148,9 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *clc_bar = item_empty + 2;
     uint64_t *drain = clc_bar + 1;
     void *clc_resp = smem + L::OFF_CLC;
-    volatile int *item_slot = reinterpret_cast<volatile int *>(smem + L::OFF_MISC);  // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC + 8);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 12);
+    volatile int *item_slot = reinterpret_cast<volatile int *>(smem + L::OFF_MISC);  // [2][4]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC + 32);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 36);
+    const bool packed = GENERAL && p.varlen;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -198,17 +226,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // publish the block to the other roles (two slots)
                 const int slot = k & 1;
                 if (k >= 2 && !mbar_wait(&item_empty[slot], ((k >> 1) - 1) & 1, abort_flag, p.status, 60)) break;
-                item_slot[slot] = item;
-                mbar_arrive(&item_full[slot]);  // release: the slot write is seen by every waiter
+                // the block's sequence: packed batches read its bounds once, here
+                int row0 = 0, n = p.N;
+                if (packed && item >= 0) {
+                    int plane, t_lin;
+                    grid_decode(item, p.planes, p.nblk, p.group, plane, t_lin);
+                    const int b = plane / p.Hq;
+                    row0 = p.cu_seqlens[b];
+                    n = p.cu_seqlens[b + 1] - row0;
+                    if (n < 0 || n > p.N || row0 < 0 || row0 + n > p.total) {
+                        record_bad_args(p.status);
+                        row0 = 0;
+                        n = 0;  // no work for this block
+                    }
+                }
+                item_slot[4 * slot] = item;
+                item_slot[4 * slot + 1] = row0;
+                item_slot[4 * slot + 2] = n;
+                mbar_arrive(&item_full[slot]);  // release: the slot writes are seen by every waiter
                 if (item < 0) break;
                 // ask for the next block while this one's tiles load
                 mbar_arrive_expect_tx(clc_bar, 16);
                 clc_try_cancel(clc_resp, clc_bar);
                 clc_pending = true;
-                const Block blk = decode_block(item, p);
+                const Block blk = decode_block(item, row0, n, p);
                 const int b = blk.bh / p.Hq;
                 const int h = blk.bh - b * p.Hq;
-                const int kv_plane = b * p.Hkv + h / (p.Hq / p.Hkv);
+                const int hk = h / (p.Hq / p.Hkv);
+                const int kv_plane = b * p.Hkv + hk;
                 // Q_x: its buffer is free once the previous block's last S_x MMA has completed
                 for (int x = 0; x < 2 && ok; ++x) {
                     if ((x ? blk.nB : blk.nA) == 0) continue;
@@ -217,14 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&q_full[x], L::TILE);
+                    const int qr = blk.q0a + x * kBM;
                     for (int bx = 0; bx < L::NBOX; ++bx)
                         tma_load_3d(smem + L::OFF_Q + x * L::TILE + bx * L::BOX, &tm_q, &q_full[x], bx * 64,
-                                    blk.q0a + x * kBM, blk.bh);
+                                    packed ? h : qr, packed ? row0 + qr : blk.bh);
                     ++nq[x];
                 }
                 // K_j then V_j, continuing the ring positions of earlier blocks
-                for (int j = 0; ok && j < blk.nmax; ++j) {
-                    const int u = u_base + j;
+                for (int j = blk.jA0; ok && j < blk.nmax; ++j) {
+                    const int u = u_base + (j - blk.jA0);
                     const int ks = u % L::KS;
                     if (u >= L::KS && !mbar_wait(&k_empty[ks], ((u / L::KS) + 1) & 1, abort_flag, p.status, 62)) {
                         ok = false;
@@ -233,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&k_full[ks], L::TILE);
                     for (int bx = 0; bx < L::NBOX; ++bx)
                         tma_load_3d(smem + L::OFF_K + ks * L::TILE + bx * L::BOX, &tm_k, &k_full[ks], bx * 64,
-                                    j * kBN, kv_plane);
+                                    packed ? hk : j * kBN, packed ? row0 + j * kBN : kv_plane);
                     ++nk;
                     const int vs = u % L::VS;
                     if (u >= L::VS && !mbar_wait(&v_empty[vs], ((u / L::VS) + 1) & 1, abort_flag, p.status, 63)) {
@@ -243,11 +289,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&v_full[vs], L::TILE);
                     for (int bx = 0; bx < L::NBOX; ++bx)
                         tma_load_3d(smem + L::OFF_V + vs * L::TILE + bx * L::BOX, &tm_v, &v_full[vs], bx * 64,
-                                    j * kBN, kv_plane);
+                                    packed ? hk : j * kBN, packed ? row0 + j * kBN : kv_plane);
                     ++nv;
                 }
                 if (!ok) break;
-                u_base += blk.nmax;
+                u_base += blk.nmax - blk.jA0;
                 // the next block: the one whose CTA was canceled, or none
                 if (!mbar_wait(clc_bar, clc_n & 1, abort_flag, p.status, 64)) break;
                 ++clc_n;
@@ -324,11 +370,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; ok; ++k) {
                 const int slot = k & 1;
                 if (!mbar_wait(&item_full[slot], (k >> 1) & 1, abort_flag, p.status, 68)) break;
-                const int item = item_slot[slot];
+                const int item = item_slot[4 * slot];
+                const int row0 = item_slot[4 * slot + 1], n = item_slot[4 * slot + 2];
                 mbar_arrive(&item_empty[slot]);
                 if (item < 0) break;
-                const Block blk = decode_block(item, p);
+                const Block blk = decode_block(item, row0, n, p);
                 const int nA = blk.nA, nB = blk.nB, nmax = blk.nmax;
+                if constexpr (GENERAL) {
+                    // the plain forward's general schedule: per K/V tile j (stream
+                    // position u), for each tile x that has work there,
+                    // O_x += P_x V_j, then S_x(j+1); a tile whose window starts one
+                    // K/V tile later has its first S issued in the step before
+                    if (nmax == 0) continue;  // empty block
+                    const int jA0 = blk.jA0, jB0 = blk.jB0;
+                    if (!(ok = wait_q(0) && wait_k(u_base))) break;
+                    issue_s(0, u_base);
+                    if (nA - jA0 == 1) mma_commit(&q_empty[0]);
+                    if (nB > 0 && jB0 == jA0) {
+                        if (!(ok = wait_q(1))) break;
+                        issue_s(1, u_base);
+                        if (nB - jB0 == 1) mma_commit(&q_empty[1]);
+                    }
+                    mma_commit(&k_empty[u_base % L::KS]);
+                    for (int j = jA0; ok && j < nmax; ++j) {
+                        const int u = u_base + (j - jA0);
+                        if (!mbar_wait(&v_full[u % L::VS], (u / L::VS) & 1, abort_flag, p.status, 69)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        for (int x = 0; x < 2; ++x) {
+                            const int nx = x ? nB : nA;
+                            const int jx0 = x ? jB0 : jA0;
+                            if (nx == 0 || j < jx0 - 1 || j >= nx) continue;
+                            if (j >= jx0) {
+                                if (!issue_pv(x, j == jx0, u)) { ok = false; break; }
+                                if (j + 1 == nx) mma_commit(&o_final[x]);
+                            }
+                            if (j + 1 < nx) {
+                                // S_x(j+1) overwrites P_x(j), which the MMAs just issued read first
+                                if (j + 1 == jx0 && !wait_q(x)) { ok = false; break; }
+                                if (!wait_k(u + 1)) { ok = false; break; }
+                                issue_s(x, u + 1);
+                                if (j + 2 == nx) mma_commit(&q_empty[x]);
+                            }
+                        }
+                        if (!ok) break;
+                        mma_commit(&v_empty[u % L::VS]);
+                        if (j + 1 < nmax) mma_commit(&k_empty[(u + 1) % L::KS]);
+                    }
+                    u_base += nmax - jA0;
+                    continue;
+                }
                 // first S of both tiles (the previous block's last P.V MMAs run first)
                 if (nA > 0) {
                     if (!(ok = wait_q(0) && wait_k(u_base))) break;
@@ -398,18 +491,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = k & 1;
             const bool got = mbar_wait(&item_full[slot], (k >> 1) & 1, abort_flag, p.status, 70);
             if (!__all_sync(0xffffffffu, got)) break;
-            const int item = item_slot[slot];
+            const int item = item_slot[4 * slot];
+            const int row0 = item_slot[4 * slot + 1], n = item_slot[4 * slot + 2];
             __syncwarp();
             if (lane == 0) mbar_arrive(&item_empty[slot]);
             if (item < 0) break;
-            const Block blk = decode_block(item, p);
+            const Block blk = decode_block(item, row0, n, p);
             const int q0 = blk.q0a + x * kBM;
             const int nx = x ? blk.nB : blk.nA;
+            const int jx0 = GENERAL ? (x ? blk.jB0 : blk.jA0) : 0;
             if (nx == 0) continue;
+            const int win = GENERAL ? p.window : 0;
             float m_ref = -INFINITY;
             float l_sum = 0.0f;    // sum of the rounded P fed to the MMA: normalises O
             float l_exact = 0.0f;  // sum of the unrounded P: gives L
-            for (int j = 0; j < nx; ++j) {
+            for (int j = jx0; j < nx; ++j) {
                 const bool got_s = mbar_wait(&s_full[x], gs & 1, abort_flag, p.status, 71);
                 if (!__all_sync(0xffffffffu, got_s)) { ok = false; break; }
                 ++gs;
@@ -425,11 +521,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait_x32(s + 64);
                 tmem_ld_wait_x32(s + 96);
                 const int kv0 = j * kBN;
-                if ((kv0 + kBN > p.N) || (p.causal && kv0 + kBN - 1 > q0)) {
-                    const int hi = p.causal ? min(p.N, q0 + row + 1) : p.N;
+                if ((kv0 + kBN > n) || (p.causal && kv0 + kBN - 1 > q0) || (win > 0 && kv0 < q0 + kBM - win)) {
+                    // visible: lo <= key < hi
+                    const int hi = p.causal ? min(n, q0 + row + 1) : n;
+                    const int lo = win > 0 ? q0 + row - win + 1 : 0;
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
-                        if (kv0 + c >= hi) s[c] = __float_as_uint(-INFINITY);
+                        if (kv0 + c >= hi || kv0 + c < lo) s[c] = __float_as_uint(-INFINITY);
                 }
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -450,7 +548,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rescale = true;
                 }
                 __syncwarp();
-                const float2 neg_m = make_float2(-m_ref, -m_ref);
+                // a row that has seen no visible key yet (its window starts in a
+                // later tile) keeps m_ref = -inf: use 0, so that its masked
+                // scores give P = 0 rather than -inf - (-inf)
+                const float m_use = (GENERAL && m_ref == -INFINITY) ? 0.0f : m_ref;
+                const float2 neg_m = make_float2(-m_use, -m_use);
                 const float2 sl2x2 = make_float2(sl2, sl2);
                 float2 lr01 = make_float2(0.f, 0.f), lr23 = lr01, le01 = lr01, le23 = lr01;
                 constexpr int CH = 32;
@@ -486,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l_sum += (lr01.x + lr01.y) + (lr23.x + lr23.y);
                 l_exact += (le01.x + le01.y) + (le23.x + le23.y);
-                // O_x holds this block's P(0..j-1) V; warp-uniform rescale
-                if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
+                // O_x holds this block's P(jx0..j-1) V; warp-uniform rescale
+                if (j > jx0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t o[32];
@@ -510,8 +612,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++nf;
             tc_fence_after();
             const float inv_l = 1.0f / l_sum;
-            const bool in = q0 + row < p.N;
-            const size_t r = (size_t)blk.bh * p.N + q0 + row;
+            const bool in = q0 + row < n;
+            // O row r of [B][Hq][N][d] (dense) or [total][Hq][d] (packed); LSE
+            // entry li of [B][Hq][N] or [Hq][total]
+            size_t r = (size_t)blk.bh * p.N + q0 + row, li = r;
+            if (packed) {
+                const int h = blk.bh % p.Hq;
+                r = (size_t)(row0 + q0 + row) * p.Hq + h;
+                li = (size_t)h * p.total + row0 + q0 + row;
+            }
             uint8_t *dst = static_cast<uint8_t *>(p.o) + r * (D * 2);
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -530,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st_global_v8(dst + c0 * 2 + 32, w + 8);
                 }
             }
-            if (in) p.lse[r] = (m_ref + log2f(l_exact)) * 0.69314718055994530942f;
+            if (in) p.lse[li] = (m_ref + log2f(l_exact)) * 0.69314718055994530942f;
             // the next block's first P.V overwrites O_x only after this
             // warpgroup's next p_full arrival, which follows these loads
         }
@@ -547,19 +656,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool BF16>
 cudaError_t launch_fwd_persist_t(const FwdArgs &a, cudaStream_t st) {
+    const bool general = a.window > 0 || a.lay.varlen;
     using L = PersistLayout<D>;
     const CUtensorMapDataType dt = BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap tq, tk, tv;
     if (!make_tmap_tiles(&tq, a.q, dt, D, a.lay, a.Hq, kBM) || !make_tmap_tiles(&tk, a.k, dt, D, a.lay, a.Hkv, kBN) ||
         !make_tmap_tiles(&tv, a.v, dt, D, a.lay, a.Hkv, kBN))
         return cudaErrorInvalidValue;
-    auto kernel = fwd_persist_kernel<D, BF16>;
+    auto kernel = general ? fwd_persist_kernel<D, BF16, true> : fwd_persist_kernel<D, BF16, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     PersistParams p;
     p.o = a.o;
     p.lse = a.lse;
     p.status = device_status_ptr();
+    p.cu_seqlens = a.lay.cu_seqlens;
+    p.varlen = a.lay.varlen;
+    p.total = a.lay.total;
+    p.window = a.window;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
     p.N = a.N;
@@ -579,7 +693,7 @@ cudaError_t launch_fwd_persist_t(const FwdArgs &a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_fwd_persist(const FwdArgs &a, cudaStream_t st) {
-    if (a.window > 0 || a.lay.varlen || a.o_f32) return cudaErrorInvalidValue;  // dense, 16-bit output only
+    if (a.o_f32) return cudaErrorInvalidValue;  // 16-bit output only
     if (reinterpret_cast<uintptr_t>(a.o) & 31u) return cudaErrorInvalidValue;     // 32-byte row stores
     if (a.d == 128) return a.bf16 ? launch_fwd_persist_t<128, true>(a, st) : launch_fwd_persist_t<128, false>(a, st);
     if (a.d == 64) return a.bf16 ? launch_fwd_persist_t<64, true>(a, st) : launch_fwd_persist_t<64, false>(a, st);

@@ -63,7 +63,9 @@ typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype_t;
  *   o [B][Hq][N][d]                       (out, element type `dtype`)
  *   lse [B][Hq][N]                        (out, fp32, natural log)
  * Short sequences (N <= 2048) run the kernel of fa_fwd_persistent, longer
- * ones one CTA per 256-row block; both give the same bits.
+ * ones one CTA per 256-row block; both give the same bits.  fa_fwd_local
+ * with window <= 2048 and fa_fwd_varlen with max_seqlen <= 2048 (or a
+ * window <= 2048) use the persistent kernel in the same way.
  */
 fa_status_t fa_fwd(const void *q, const void *k, const void *v, void *o,
                    float *lse, int B, int Hq, int Hkv, int N, int d,

@@ -95,3 +95,38 @@ def test_bad_offsets_reported_not_faulted(cuda_lib):
     torch.cuda.synchronize()
     assert _lib.fa_get_device_status() == _lib.FA_ERR_INVALID_ARG
     assert _lib.fa_get_device_status() == _lib.FA_OK  # reading clears it
+
+
+@pytest.mark.parametrize("lengths,Hq,Hkv,d,causal,window", [
+    ([0, 1, 127, 128, 129, 255, 256, 257, 1000, 0, 2048], 4, 2, 128, True, 0),
+    ([5, 300, 1, 2049], 2, 2, 64, False, 0),
+    ([700, 0, 3000, 64], 4, 1, 128, True, 200),
+])
+def test_varlen_persistent_and_plain_kernels_agree(cuda_lib, lengths, Hq, Hkv, d, causal, window):
+    """fa_fwd_varlen runs the persistent forward when no row sees more than
+    2048 keys (max_seqlen or the window) and O is 32-byte aligned, else one
+    CTA per block: for the same batch both give the same bits (empty
+    sequences and blocks past a sequence's end included), and the oracle's
+    values within tolerance."""
+    x = make_varlen(lengths, Hq, Hkv, d, torch.bfloat16, seed=len(lengths) + d, with_grad=False)
+    q, k, v = (x[n].cuda().contiguous() for n in ("q", "k", "v"))
+    cu = x["cu_seqlens"].cuda()
+    total = q.shape[0]
+    scale = d ** -0.5
+    outs = []
+    for align16 in (False, True):
+        if align16:
+            buf = torch.empty(q.numel() + 8, dtype=q.dtype, device="cuda")
+            o = buf[8:].view(q.shape)
+            assert o.data_ptr() % 32 == 16
+        else:
+            o = torch.empty_like(q)
+        lse = torch.empty((Hq, total), dtype=torch.float32, device="cuda")
+        _lib.fa_fwd_varlen(q, k, v, o, lse, cu, max(lengths), causal, scale, window)
+        torch.cuda.synchronize()
+        assert _lib.fa_get_device_status() == _lib.FA_OK
+        outs.append((o, lse))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    ro, rl = oracle.attention_fwd_varlen(x["q"], x["k"], x["v"], x["cu_seqlens"], causal, scale, window)
+    check_o(outs[0][0], ro)
+    check_lse(outs[0][1], rl)

@@ -89,3 +89,38 @@ def test_window_rejects_zero(cuda_lib):
     with pytest.raises(_lib.FAError) as e:
         _lib.fa_fwd_local(q, k, v, o, lse, 0, 0.125)
     assert e.value.status == _lib.FA_ERR_INVALID_ARG
+
+
+def _o16(q):
+    """An output buffer only 16-byte aligned: fa_fwd_local then runs the
+    one-CTA-per-block kernel instead of the persistent one (32-byte stores)."""
+    buf = torch.empty(q.numel() + 8, dtype=q.dtype, device=q.device)
+    o = buf[8:].view(q.shape)
+    assert o.data_ptr() % 32 == 16
+    return o
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,dtype,window", [
+    (1, 4, 2, 1500, 128, torch.bfloat16, 1),
+    (2, 4, 1, 1100, 128, torch.float16, 200),
+    (1, 2, 2, 3000, 64, torch.bfloat16, 1000),
+    (1, 2, 2, 2600, 128, torch.bfloat16, 2048),  # the largest window routed to the persistent kernel
+    (1, 2, 2, 2600, 128, torch.bfloat16, 2049),  # the smallest one that is not
+])
+def test_window_persistent_and_plain_kernels_agree(cuda_lib, B, Hq, Hkv, N, d, dtype, window):
+    """The two forward kernels fa_fwd_local chooses between (persistent for
+    windows up to 2048 keys with a 32-byte-aligned O, else one CTA per
+    block) compute every block the same way: the same bits, and both within
+    the tolerance of the oracle."""
+    x = make_custom(B, Hq, Hkv, N, d, dtype, seed=N + 3 * window, with_grad=False)
+    scale = d ** -0.5
+    q, k, v, o, lse = _fwd(x, window, scale)
+    o2 = _o16(q)
+    lse2 = torch.empty_like(lse)
+    _lib.fa_fwd_local(q, k, v, o2, lse2, window, scale)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    ro, rl = oracle.attention_fwd(x["q"], x["k"], x["v"], True, scale, window=window)
+    check_o(o, ro)
+    check_lse(lse, rl)
