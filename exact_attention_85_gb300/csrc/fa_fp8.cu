@@ -513,15 +513,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P.V of this tile), and P_x(j) V is issued only after p_full;
             // warp-uniform branch, lanes that keep their max use alpha = 1
             if (j >= 1 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-                for (int c0 = 0; c0 < kD; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld_x32(lane_base + col_o + c0, o);
-                    tmem_ld_wait_x32(o);
+                // one tensor-memory round trip: the S registers are free again
+                uint32_t o[kD];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                    tmem_st_x32(lane_base + col_o + c0, o);
+                for (int c0 = 0; c0 < kD; c0 += 32) tmem_ld_x32(lane_base + col_o + c0, o + c0);
+#pragma unroll
+                for (int c0 = 0; c0 < kD; c0 += 32) tmem_ld_wait_x32(o + c0);
+#pragma unroll
+                for (int c = 0; c < kD; c += 2) {
+                    const float2 r = fmul2(make_float2(__uint_as_float(o[c]), __uint_as_float(o[c + 1])),
+                                           make_float2(alpha, alpha));
+                    o[c] = __float_as_uint(r.x);
+                    o[c + 1] = __float_as_uint(r.y);
                 }
+#pragma unroll
+                for (int c0 = 0; c0 < kD; c0 += 32) tmem_st_x32(lane_base + col_o + c0, o + c0);
             }
             tmem_st_wait();
             tc_fence_before();
