@@ -465,16 +465,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, w3)) { ok = false; break; }
             tc_fence_after();
             uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
-            uint32_t dpv[32];  // dP^T of two chunks at a time
+            // dP^T one chunk at a time, each chunk's load issued before the
+            // previous chunk's arithmetic (the wait then finds it done)
+            uint32_t dpv[2][16];
             uint32_t ddk[kNCH][8];  // packed dS^T, kept for the shared-memory copy
+            tmem_ld_x16(lane_base + kColDP + q0w, dpv[0]);
 #pragma unroll
             for (int ch = 0; ch < kNCH; ++ch) {
                 const int qc = q0w + ch * 16;
-                if ((ch & 1) == 0) {
-                    tmem_ld_x32(lane_base + kColDP + qc, dpv);
-                    tmem_ld_wait_x32(dpv);
-                }
-                const uint32_t *dp = dpv + 16 * (ch & 1);
+                tmem_ld_wait_x16(dpv[ch & 1]);  // the only load outstanding
+                if (ch + 1 < kNCH) tmem_ld_x16(lane_base + kColDP + qc + 16, dpv[(ch + 1) & 1]);
+                const uint32_t *dp = dpv[ch & 1];
                 float dv_[16];  // the chunk's 16 values of D
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {

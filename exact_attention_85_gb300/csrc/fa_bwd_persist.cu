@@ -508,16 +508,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!__all_sync(0xffffffffu, w3)) { ok = false; break; }
                 tc_fence_after();
                 uint8_t *ds_row = smem + L::OFF_DS + hf * L::DS_BOX + c * 128;
-                uint32_t dpv[32];
+                uint32_t dpv[2][16];  // dP^T one chunk at a time, loaded one chunk ahead
                 uint32_t ddk[kNCH][8];
+                tmem_ld_x16(lane_base + kColDP + q0w, dpv[0]);
 #pragma unroll
                 for (int ch = 0; ch < kNCH; ++ch) {
                     const int qc = q0w + ch * 16;
-                    if ((ch & 1) == 0) {
-                        tmem_ld_x32(lane_base + kColDP + qc, dpv);
-                        tmem_ld_wait_x32(dpv);
-                    }
-                    const uint32_t *dp = dpv + 16 * (ch & 1);
+                    tmem_ld_wait_x16(dpv[ch & 1]);  // the only load outstanding
+                    if (ch + 1 < kNCH) tmem_ld_x16(lane_base + kColDP + qc + 16, dpv[(ch + 1) & 1]);
+                    const uint32_t *dp = dpv[ch & 1];
                     float dv_[16];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
