@@ -15,6 +15,8 @@ the first left in the shared buffer):
     fa_bwd's status codes.
 
 This file is named so that pytest collects it last."""
+import gc
+
 import pytest
 import torch
 
@@ -75,12 +77,20 @@ def test_noalloc_matches_oracle_and_fa_bwd_on_two_calls(cuda_lib, B, Hq, Hkv, N,
     for call in range(2):
         got = [torch.full_like(q, float("nan")), torch.full_like(k, float("nan")), torch.full_like(v, float("nan"))]
         torch.cuda.synchronize()
-        alloc0 = torch.cuda.memory_allocated()
-        free0, _ = torch.cuda.mem_get_info()
-        _lib.fa_bwd_noalloc(q, k, v, o, lse, dO, *got, causal, scale)
-        torch.cuda.synchronize()
-        free1, _ = torch.cuda.mem_get_info()
-        assert torch.cuda.memory_allocated() == alloc0
+        # the collector is paused so that no unrelated tensor is freed
+        # between the two readings
+        gc.collect()
+        gc.disable()
+        try:
+            alloc0 = torch.cuda.memory_allocated()
+            free0, _ = torch.cuda.mem_get_info()
+            _lib.fa_bwd_noalloc(q, k, v, o, lse, dO, *got, causal, scale)
+            torch.cuda.synchronize()
+            free1, _ = torch.cuda.mem_get_info()
+            alloc1 = torch.cuda.memory_allocated()
+        finally:
+            gc.enable()
+        assert alloc1 == alloc0
         if call == 1:
             assert free1 == free0, f"device free bytes changed across the call: {free0} -> {free1}"
         assert _lib.fa_get_device_status() == _lib.FA_OK
