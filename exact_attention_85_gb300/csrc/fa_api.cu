@@ -161,8 +161,9 @@ fa_status_t check_shape(int B, int Hq, int Hkv, int N, int d, float scale, long 
     if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
     if (!(scale > 0.0f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    const long long elems = rows * Hq * d;  // the largest tensor (Hq >= Hkv)
-    if (elems > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
+    // rows and (batch x head) planes are counted in 32 bits; element offsets
+    // are 64-bit everywhere, so a tensor may hold more than 2^31 elements
+    if (rows > 0x7FFFFFFFll || (long long)B * Hq > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
     // 1-D grid of (Q tiles x heads x batch) CTAs
     if ((long long)((N + 127) / 128) * B * Hq > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
     return FA_OK;
@@ -307,8 +308,7 @@ fa_status_t check_varlen(const int *cu_seqlens, int B, int max_seqlen, int total
     if (!cu_seqlens || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_INVALID_ARG;
     if (B < 1 || max_seqlen < 1 || total < 1 || Hq < 1 || Hkv < 1) return FA_ERR_INVALID_ARG;
     if (window < 0 || (window > 0 && !causal)) return FA_ERR_INVALID_ARG;
-    if ((long long)total * (Hq > Hkv ? Hq : Hkv) * d > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
-    return FA_OK;
+    return FA_OK;  // sizes: check_shape, with the packed total as the row count
 }
 }  // namespace
 
@@ -354,7 +354,6 @@ fa_status_t fa_hadamard_quant_fp8(const void *x_bf16, const float *signs, void *
     if (!x_bf16 || !x_e4m3 || !descale || rows < 1) return FA_ERR_INVALID_ARG;
     if (!aligned16(x_bf16) || !aligned16(x_e4m3) || (signs && !aligned16(signs))) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-    if ((long long)rows * d > 0x7FFFFFFFll) return FA_ERR_UNSUPPORTED;
     if (!workspace || workspace_bytes < fa_hadamard_quant_workspace_bytes(rows, d) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FA_ERR_WORKSPACE;

@@ -20,8 +20,9 @@
  * Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).  All
  *           compute entry points are asynchronous on that stream.
  * Sizes.    1 <= N; d in {64, 128}; Hq % Hkv == 0; B, Hq, Hkv >= 1; the
- *           element count B*Hq*N*d must fit in 2^31 - 1 per tensor (packed
- *           batches: total*Hq*d, whatever B * max_seqlen is).
+ *           row count B*N (packed batches: total) and B*Hq at most 2^31 - 1,
+ *           and ceil(N / 128) * B * Hq at most 2^31 - 1 (one CTA per 128-row
+ *           tile and head); a tensor may hold more than 2^31 elements.
  * Errors.   Invalid arguments are reported before anything is launched
  *           (FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_WORKSPACE) and
  *           leave every output untouched.  A failed launch returns

@@ -63,7 +63,8 @@ def test_fwd_argument_validation(lib):
     assert _fwd(lib, dtype=7) == 1
     assert _fwd(lib, d=96) == 2                # unsupported head dim
     assert _fwd(lib, d=256) == 2
-    assert _fwd(lib, B=1 << 12, Hq=1 << 10, Hkv=1, N=1 << 12) == 2  # too many elements
+    assert _fwd(lib, B=1 << 16, Hq=2, Hkv=1, N=1 << 16) == 2    # B * N rows beyond 2^31 - 1
+    assert _fwd(lib, B=1 << 12, Hq=1 << 12, Hkv=1, N=1 << 16) == 2  # more CTAs than a 1-D grid holds
 
 
 def test_persistent_forward_needs_32_byte_aligned_output(lib):
@@ -180,7 +181,7 @@ def test_varlen_argument_validation(lib):
     assert fwd(window=4, causal=0) == 1     # a window needs the causal mask
     assert fwd(Hq=3, Hkv=2) == 1
     assert fwd(d=32) == 2
-    assert fwd(total=1 << 24, Hq=1 << 4) == 2   # total * H * d beyond 2^31 - 1
+    assert fwd(max_seqlen=1 << 30, Hq=1 << 9) == 2   # ceil(max_seqlen / 128) * B * Hq CTAs beyond 2^31 - 1
     assert fwd(q=FAKE + 8) == 1
     for det in (0, 1):
         need = lib.fa_bwd_varlen_workspace_bytes(24, 2, 128, det)
@@ -195,16 +196,19 @@ def test_varlen_argument_validation(lib):
 def test_packed_batch_size_limit_counts_packed_rows(lib):
     """A packed batch is sized by its total rows, not by B * max_seqlen: 64
     sequences with one of 32768 rows and 3000 rows in all pass the size check
-    (and here stop at the undersized workspace, before any launch)."""
+    (and here stop at the undersized workspace, before any launch); so do
+    more than 2^31 elements per tensor."""
     B, max_seqlen, total, Hq, d = 64, 32768, 3000, 16, 128
     assert B * max_seqlen * Hq * d > 2 ** 31                      # the old, dense-shaped count
     need = lib.fa_bwd_varlen_workspace_bytes(total, Hq, d, 0)
     args = [FAKE] * 9 + [FAKE, B, max_seqlen, total, Hq, Hq, d, 1, 0, 0.1, 1, 0]
     assert lib.fa_bwd_varlen(*args, FAKE, need - 256, None) == 3
-    # more packed rows than the limit allows are still refused
+    # total * Hq * d beyond 2^31 elements is accepted (64-bit offsets): the
+    # call gets as far as the workspace check
     big = 2 ** 31 // (Hq * d) + 1
+    need_big = lib.fa_bwd_varlen_workspace_bytes(big, Hq, d, 0)
     args_big = [FAKE] * 9 + [FAKE, B, max_seqlen, big, Hq, Hq, d, 1, 0, 0.1, 1, 0]
-    assert lib.fa_bwd_varlen(*args_big, FAKE, 1 << 40, None) == 2
+    assert lib.fa_bwd_varlen(*args_big, FAKE, need_big - 256, None) == 3
 
 
 def test_packed_batch_wrappers_marshal_arguments(monkeypatch):
