@@ -67,90 +67,125 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v) {
 }
 
 // --------------------------------------------- Hadamard + quantise kernels
-// Row layout: LPR = D / 8 lanes per row, 8 consecutive values per lane
-// (one 16-byte load), so a warp holds 32 / LPR rows.  Butterflies for
-// strides 1, 2, 4 run inside a lane; strides 8 .. D/2 pair lanes whose
-// in-row index differs in one bit.
+// Row layout: 4 lanes per row; lane j (0..3) holds the 16-byte chunks
+// 4 k + j (k = 0 .. D/32 - 1) of its row, 8 values each, so a warp holds 8
+// rows and every load instruction covers 64 contiguous bytes of each row.
+// In the row index v = 8 (4 k + j) + e the butterflies for the bits of e and
+// of k run inside a lane, those for the two bits of j across the 4 lanes (2
+// shuffle stages; with one chunk per lane and 16 lanes per row it took 4).
 
 template <int D>
-__device__ __forceinline__ void hadamard_row(float (&x)[8], int sub) {
+struct HqShape {
+    static constexpr int CPL = D / 32;   // 16-byte chunks per lane
+    static constexpr int VPL = CPL * 8;  // values per lane
+    static constexpr int RPW = 8;        // rows per warp
+    // groups of 8 rows per warp and trip, all loaded before any is
+    // transformed, so several loads per warp are in flight
+    static constexpr int KU = D == 128 ? 2 : 4;
+};
+
+// The transform on packed pairs w[p] = (v[2p], v[2p + 1]): stride 1 inside a
+// pair, strides >= 2 as packed fp32 adds of whole pairs, the two cross-lane
+// stages as one packed fma each (x + other, or other - x in the upper lane).
+// On bf16 inputs every partial sum is exact in fp32, so any stage order
+// gives the same result.  The 1/sqrt(d) factor is left to the caller.
+template <int D>
+__device__ __forceinline__ void hadamard_pairs(float2 (&w)[HqShape<D>::VPL / 2], int j) {
+    constexpr int NP = HqShape<D>::VPL / 2;
 #pragma unroll
-    for (int s = 1; s < 8; s <<= 1) {
+    for (int p = 0; p < NP; ++p) {
+        const float a = w[p].x, b = w[p].y;
+        w[p] = make_float2(a + b, a - b);
+    }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if ((i & s) == 0) {
-                const float a = x[i], b = x[i + s];
-                x[i] = a + b;
-                x[i + s] = a - b;
+    for (int s = 1; s < NP; s <<= 1) {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            if ((p & s) == 0) {
+                const float2 a = w[p], b = w[p + s];
+                w[p] = fadd2(a, b);
+                w[p + s] = fsub2(a, b);
             }
         }
     }
 #pragma unroll
-    for (int m = 1; m < D / 8; m <<= 1) {
-        const bool upper = (sub & m) != 0;
+    for (int m = 1; m < 4; m <<= 1) {
+        const float sg = (j & m) ? -1.0f : 1.0f;
+        const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float other = __shfl_xor_sync(0xffffffffu, x[i], m);
-            x[i] = upper ? (other - x[i]) : (x[i] + other);
+        for (int p = 0; p < NP; ++p) {
+            const float2 other = make_float2(__shfl_xor_sync(0xffffffffu, w[p].x, m),
+                                             __shfl_xor_sync(0xffffffffu, w[p].y, m));
+            w[p] = ffma2(w[p], sg2, other);
         }
     }
-    constexpr float inv_sqrt_d = D == 128 ? 0.08838834764831845f : 0.125f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] *= inv_sqrt_d;
 }
 
-// Loads one 16-byte slice (8 values) of `row`, or zeros past the end.
+// This lane's chunks of `row` (zeros past the end).
 template <int D>
-__device__ __forceinline__ uint4 load_slice(const uint4 *__restrict__ x, long row, long rows, int sub) {
-    return row < rows ? x[row * (D / 8) + sub] : make_uint4(0u, 0u, 0u, 0u);
+__device__ __forceinline__ void load_chunks(const uint4 *__restrict__ x, long row, long rows, int j,
+                                            uint4 (&u)[HqShape<D>::CPL]) {
+#pragma unroll
+    for (int k = 0; k < HqShape<D>::CPL; ++k)
+        u[k] = row < rows ? x[row * (D / 8) + 4 * k + j] : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Widens a slice to floats, applies the signs and the row transform.
+// Widens the chunks to float pairs with the signs applied (a flip of each
+// bf16 sign bit, `flip` holding the bits per 32-bit word) and transforms
+// them when signs are given; the 1/sqrt(d) factor is not applied.
 template <int D>
-__device__ __forceinline__ void rotate_slice(uint4 u, const float *__restrict__ signs, int sub, float (&v)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ void rotate_raw(const uint4 (&u)[HqShape<D>::CPL], const uint32_t (&flip)[HqShape<D>::VPL / 2],
+                                          bool use_signs, int j, float2 (&w)[HqShape<D>::VPL / 2]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = unpack2<true>(w[i]);
-        v[2 * i] = f.x;
-        v[2 * i + 1] = f.y;
-    }
-    if (signs) {
+    for (int k = 0; k < HqShape<D>::CPL; ++k) {
+        const uint32_t q[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] *= signs[sub * 8 + i];
-        hadamard_row<D>(v, sub);  // all lanes of the warp take part
+        for (int i = 0; i < 4; ++i) w[4 * k + i] = unpack2<true>(q[i] ^ flip[4 * k + i]);
     }
+    if (use_signs) hadamard_pairs<D>(w, j);  // all lanes of the warp take part
+}
+
+// This lane's sign flips: for the pair of values 8 (4 k + j) + 2 i, + 1, the
+// sign bits of the two bf16 halves of a word.
+template <int D>
+__device__ __forceinline__ void load_flips(const float *__restrict__ signs, int j, uint32_t (&flip)[HqShape<D>::VPL / 2]) {
+#pragma unroll
+    for (int k = 0; k < HqShape<D>::CPL; ++k)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int v = 8 * (4 * k + j) + 2 * i;
+            flip[4 * k + i] = signs ? ((signs[v] < 0.0f ? 0x8000u : 0u) | (signs[v + 1] < 0.0f ? 0x80000000u : 0u)) : 0u;
+        }
 }
 
 __global__ void hq_zero_kernel(float *amax) { *amax = 0.0f; }
 
-// Each warp takes kU groups of rows per trip and issues all their loads before
-// transforming any, so several loads per warp are in flight.
-constexpr int kU = 8;
-
 template <int D>
 __global__ void __launch_bounds__(256) hq_amax_kernel(const uint4 *__restrict__ x, const float *__restrict__ signs,
                                                       float *__restrict__ amax, long rows) {
-    constexpr int LPR = D / 8;
-    constexpr int RPW = 32 / LPR;
+    using S = HqShape<D>;
+    constexpr int kU = S::KU;
     const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int sub = lane % LPR;
-    float m = 0.0f;
+    const int j = lane & 3;
+    uint32_t flip[S::VPL / 2];
+    load_flips<D>(signs, j, flip);
+    float m = 0.0f;  // max |v| before the 1/sqrt(d) factor (applied once below: the order is the same)
     // warp-uniform trip count: the shuffles inside need every lane
-    for (long base = warp_id * RPW * kU; base < rows; base += nwarps * RPW * kU) {
-        uint4 u[kU];
+    for (long base = warp_id * S::RPW * kU; base < rows; base += nwarps * S::RPW * kU) {
+        uint4 u[kU][S::CPL];
 #pragma unroll
-        for (int k = 0; k < kU; ++k) u[k] = load_slice<D>(x, base + k * RPW + lane / LPR, rows, sub);
+        for (int q = 0; q < kU; ++q) load_chunks<D>(x, base + q * S::RPW + (lane >> 2), rows, j, u[q]);
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-            float v[8];
-            rotate_slice<D>(u[k], signs, sub, v);
+        for (int q = 0; q < kU; ++q) {
+            float2 w[S::VPL / 2];
+            rotate_raw<D>(u[q], flip, signs != nullptr, j, w);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+            for (int p = 0; p < S::VPL / 2; ++p) m = fmaxf(m, fmaxf(fabsf(w[p].x), fabsf(w[p].y)));
         }
     }
+    if (signs) m *= D == 128 ? 0.08838834764831845f : 0.125f;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     __shared__ float wmax[8];
@@ -168,28 +203,38 @@ template <int D>
 __global__ void __launch_bounds__(256) hq_quant_kernel(const uint4 *__restrict__ x, const float *__restrict__ signs,
                                                        const float *__restrict__ amax, uint2 *__restrict__ x8,
                                                        float *__restrict__ descale, long rows) {
-    constexpr int LPR = D / 8;
-    constexpr int RPW = 32 / LPR;
+    using S = HqShape<D>;
+    constexpr int kU = S::KU;
     const float a = *amax;
     const float inv = a > 0.0f ? 448.0f / a : 1.0f;
     if (blockIdx.x == 0 && threadIdx.x == 0) *descale = a > 0.0f ? a / 448.0f : 1.0f;
+    const float c = signs ? (D == 128 ? 0.08838834764831845f : 0.125f) : 1.0f;  // 1/sqrt(d) of the transform
+    const float2 c2 = make_float2(c, c), inv2 = make_float2(inv, inv);
     const long warp_id = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long nwarps = ((long)gridDim.x * blockDim.x) >> 5;
     const int lane = threadIdx.x & 31;
-    const int sub = lane % LPR;
-    for (long base = warp_id * RPW * kU; base < rows; base += nwarps * RPW * kU) {
-        uint4 u[kU];
+    const int j = lane & 3;
+    uint32_t flip[S::VPL / 2];
+    load_flips<D>(signs, j, flip);
+    for (long base = warp_id * S::RPW * kU; base < rows; base += nwarps * S::RPW * kU) {
+        uint4 u[kU][S::CPL];
 #pragma unroll
-        for (int k = 0; k < kU; ++k) u[k] = load_slice<D>(x, base + k * RPW + lane / LPR, rows, sub);
+        for (int q = 0; q < kU; ++q) load_chunks<D>(x, base + q * S::RPW + (lane >> 2), rows, j, u[q]);
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-            const long row = base + k * RPW + lane / LPR;
-            float v[8];
-            rotate_slice<D>(u[k], signs, sub, v);
+        for (int q = 0; q < kU; ++q) {
+            const long row = base + q * S::RPW + (lane >> 2);
+            float2 w[S::VPL / 2];
+            rotate_raw<D>(u[q], flip, signs != nullptr, j, w);
             if (row < rows) {
-                const uint32_t lo = cvt_e4m3x2(v[0] * inv, v[1] * inv) | (cvt_e4m3x2(v[2] * inv, v[3] * inv) << 16);
-                const uint32_t hi = cvt_e4m3x2(v[4] * inv, v[5] * inv) | (cvt_e4m3x2(v[6] * inv, v[7] * inv) << 16);
-                x8[row * (D / 8) + sub] = make_uint2(lo, hi);
+#pragma unroll
+                for (int k = 0; k < S::CPL; ++k) {
+                    float2 t[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) t[i] = fmul2(fmul2(w[4 * k + i], c2), inv2);
+                    const uint32_t lo = cvt_e4m3x2(t[0].x, t[0].y) | (cvt_e4m3x2(t[1].x, t[1].y) << 16);
+                    const uint32_t hi = cvt_e4m3x2(t[2].x, t[2].y) | (cvt_e4m3x2(t[3].x, t[3].y) << 16);
+                    x8[row * (D / 8) + 4 * k + j] = make_uint2(lo, hi);
+                }
             }
         }
     }

@@ -304,7 +304,8 @@ size_t fa_hadamard_quant_workspace_bytes(long rows, int d);
  * sigma = amax(|x'|) / 448 over the whole tensor and x8 = e4m3(x' / sigma)
  * (round to nearest even, saturating).
  *   x_bf16  [rows][d] bf16 (in)
- *   signs   [d] fp32 of +-1 (in), or NULL for no rotation (plain FP8)
+ *   signs   [d] fp32 of +-1 (in; only the sign of each entry is used), or
+ *           NULL for no rotation (plain FP8)
  *   x_e4m3  [rows][d] e4m3 (out)
  *   descale one fp32 device scalar (out): sigma, so x' ~= sigma * x8
  *   workspace: >= fa_hadamard_quant_workspace_bytes(rows, d) bytes
