@@ -75,3 +75,36 @@ def test_bwd_with_16_byte_aligned_dk_dv_falls_back(cuda_lib):
     check_grad(dv, rv, "dV")
     _, dk2, dv2 = _fwd_bwd(x, True, scale)
     assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
+def test_persistent_bwd_concurrent_streams(cuda_lib):
+    """Two persistent backward passes with different inputs running at the
+    same time on two streams: each grid takes only its own not-yet-launched
+    CTAs' work items, so dK and dV equal the one-stream results bit for bit
+    (dQ up to the order of its atomic additions) and match the oracle."""
+    B, H, N, d = 16, 8, 512, 128
+    scale = d ** -0.5
+    xs = [make_custom(B, H, H, N, d, torch.bfloat16, seed=s) for s in (51, 52)]
+    dev = [{n: x[n].cuda().contiguous() for n in ("q", "k", "v", "dO")} for x in xs]
+    fw = []
+    for t in dev:
+        o = torch.empty_like(t["q"])
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        _lib.fa_fwd(t["q"], t["k"], t["v"], o, lse, True, scale)
+        fw.append((o, lse))
+    outs = [tuple(torch.empty_like(t[n]) for n in ("q", "k", "v")) for t in dev]
+    wss = [torch.empty(_lib.fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda") for _ in dev]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for t, (o, lse), g, ws, st in zip(dev, fw, outs, wss, streams):
+            _lib.fa_bwd(t["q"], t["k"], t["v"], o, lse, t["dO"], *g, True, scale, ws, st)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    for x, g in zip(xs, outs):
+        dq, dk, dv = _fwd_bwd(x, True, scale)
+        assert torch.equal(g[1], dk) and torch.equal(g[2], dv)
+        rq, rk, rv = oracle.attention_bwd(x["q"], x["k"], x["v"], x["dO"], True, scale)
+        check_grad(g[0], rq, "dQ")
+        check_grad(g[1], rk, "dK")
+        check_grad(g[2], rv, "dV")
