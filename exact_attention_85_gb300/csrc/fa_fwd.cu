@@ -264,8 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nB > 0 && jB0 == jA0) issue_s(1, 0);
                 mma_commit(&k_empty[0]);
             }
-            if constexpr (!GENERAL) {
-                // full causal or no mask: both tiles start at K/V tile 0
+            if (!GENERAL || win == 0) {
+                // no window (dense or packed): both tiles start at K/V tile 0
                 if (ok && nmax > 0) {
                     ok = mbar_wait(&v_full[0], 0, abort_flag, p.status, 6);
                     tc_fence_after();

@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (item < 0) break;
                 const Block blk = decode_block(item, row0, n, p);
                 const int nA = blk.nA, nB = blk.nB, nmax = blk.nmax;
-                if constexpr (GENERAL) {
+                if (GENERAL && p.window > 0) {
                     // the plain forward's general schedule: per K/V tile j (stream
                     // position u), for each tile x that has work there,
                     // O_x += P_x V_j, then S_x(j+1); a tile whose window starts one
@@ -422,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     u_base += nmax - jA0;
                     continue;
                 }
+                if (nmax == 0) continue;  // a packed block past its sequence's end
                 // first S of both tiles (the previous block's last P.V MMAs run first)
                 if (nA > 0) {
                     if (!(ok = wait_q(0) && wait_k(u_base))) break;
