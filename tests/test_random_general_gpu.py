@@ -1,0 +1,143 @@
+"""Seeded random shapes for the general paths against the fp64 oracle: the
+causal sliding window (fa_fwd_local / fa_bwd_local), packed variable-length
+batches (fa_fwd_varlen / fa_bwd_varlen, with and without a window) and the
+deterministic two-pass backward (fa_bwd_two_pass).
+
+The draws cross the dispatch boundaries of these entry points: windows of 1
+key, short windows, windows on both sides of the persistent forward's 2048
+keys and windows longer than the sequence; packed sequences of length 0, 1,
+ragged tails and lengths on both sides of 2048; GQA ratios 1-4, both head
+dimensions and both 16-bit element types; the atomic and the deterministic
+backward.  Tolerances are those of every parity test: O element-wise within
+4e-3 plus half an ulp of the output type, LSE max-abs 1e-3, gradients
+relative Frobenius <= 1e-2."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_85_gb300 import _lib
+from exact_attention_85_gb300.inputs import make_custom, make_varlen
+
+from _tol import check_grad, check_lse, check_o
+
+pytestmark = pytest.mark.gpu
+
+
+def _heads(g):
+    G = int(g.choice([1, 2, 4]))
+    Hkv = int(g.integers(1, 3))
+    return G * Hkv, Hkv
+
+
+def _elem(g):
+    d = int(g.choice([64, 128]))
+    dtype = torch.bfloat16 if g.integers(2) else torch.float16
+    return d, dtype
+
+
+def _window(g, N):
+    return int(g.choice([1, int(g.integers(2, 300)), int(g.integers(300, max(301, N + 64))),
+                         int(g.integers(1900, 2200)), N + int(g.integers(0, 50))]))
+
+
+def _check_all(what, o, lse, grads, ref_fwd, ref_bwd):
+    check_o(o, ref_fwd[0], f"{what} O")
+    check_lse(lse, ref_fwd[1], f"{what} LSE")
+    for name, got, ref in zip(("dQ", "dK", "dV"), grads, ref_bwd):
+        check_grad(got, ref, f"{what} {name}")
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_window(cuda_lib, seed):
+    g = np.random.default_rng(2000 + seed)
+    Hq, Hkv = _heads(g)
+    d, dtype = _elem(g)
+    N = int(g.choice([int(g.integers(1, 700)), int(g.integers(700, 1300)), int(g.integers(1900, 2700))]))
+    B = 1 if N > 1500 else int(g.integers(1, 3))
+    W = _window(g, N)
+    deterministic = bool(g.integers(2))
+    x = make_custom(B, Hq, Hkv, N, d, dtype, seed=seed)
+    q, k, v, dO = (x[n].cuda().contiguous() for n in ("q", "k", "v", "dO"))
+    scale = d ** -0.5
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+    _lib.fa_fwd_local(q, k, v, o, lse, W, scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    size = (_lib.fa_bwd_two_pass_workspace_bytes if deterministic else _lib.fa_bwd_workspace_bytes)(B, Hq, N, d)
+    ws = torch.empty(size, dtype=torch.uint8, device="cuda")
+    ws.fill_(0xFF)
+    _lib.fa_bwd_local(q, k, v, o, lse, dO, dq, dk, dv, W, scale, deterministic, ws)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    what = f"B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} {str(dtype)[6:]} W{W} deterministic={deterministic}"
+    _check_all(what, o, lse, (dq, dk, dv),
+               oracle.attention_fwd(x["q"], x["k"], x["v"], True, scale, window=W),
+               oracle.attention_bwd(x["q"], x["k"], x["v"], x["dO"], True, scale, window=W))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_packed_batch(cuda_lib, seed):
+    g = np.random.default_rng(3000 + seed)
+    Hq, Hkv = _heads(g)
+    d, dtype = _elem(g)
+    n_seq = int(g.integers(1, 7))
+    lengths = [int(g.choice([0, 1, int(g.integers(2, 300)), int(g.integers(300, 1200)),
+                             int(g.integers(1900, 2300))])) for _ in range(n_seq)]
+    if sum(lengths) == 0:
+        lengths[0] = int(g.integers(1, 200))
+    causal = bool(g.integers(2))
+    window = _window(g, max(lengths)) if causal and g.integers(2) else 0
+    deterministic = bool(g.integers(2))
+    x = make_varlen(lengths, Hq, Hkv, d, dtype, seed=seed)
+    q, k, v, dO = (x[n].cuda().contiguous() for n in ("q", "k", "v", "dO"))
+    cu = x["cu_seqlens"].cuda()
+    total = q.shape[0]
+    max_len = max(lengths)
+    scale = d ** -0.5
+    o = torch.empty_like(q)
+    lse = torch.empty((Hq, total), dtype=torch.float32, device="cuda")
+    _lib.fa_fwd_varlen(q, k, v, o, lse, cu, max_len, causal, scale, window)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(_lib.fa_bwd_varlen_workspace_bytes(total, Hq, d, deterministic), dtype=torch.uint8,
+                     device="cuda")
+    ws.fill_(0xFF)
+    _lib.fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu, max_len, causal, scale, deterministic, ws, window)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    what = (f"lengths {lengths} Hq{Hq} Hkv{Hkv} d{d} {str(dtype)[6:]} causal={causal} W{window} "
+            f"deterministic={deterministic}")
+    _check_all(what, o, lse, (dq, dk, dv),
+               oracle.attention_fwd_varlen(x["q"], x["k"], x["v"], x["cu_seqlens"], causal, scale, window),
+               oracle.attention_bwd_varlen(x["q"], x["k"], x["v"], x["dO"], x["cu_seqlens"], causal, scale,
+                                           window))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_two_pass_backward(cuda_lib, seed):
+    g = np.random.default_rng(4000 + seed)
+    Hq, Hkv = _heads(g)
+    d, dtype = _elem(g)
+    N = int(g.choice([int(g.integers(1, 700)), int(g.integers(700, 1300)), int(g.integers(1900, 2700))]))
+    B = 1 if N > 1500 else int(g.integers(1, 3))
+    causal = bool(g.integers(2))
+    x = make_custom(B, Hq, Hkv, N, d, dtype, seed=seed)
+    q, k, v, dO = (x[n].cuda().contiguous() for n in ("q", "k", "v", "dO"))
+    scale = d ** -0.5
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+    _lib.fa_fwd(q, k, v, o, lse, causal, scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(_lib.fa_bwd_two_pass_workspace_bytes(B, Hq, N, d), dtype=torch.uint8, device="cuda")
+    ws.fill_(0xFF)
+    _lib.fa_bwd_two_pass(q, k, v, o, lse, dO, dq, dk, dv, causal, scale, ws)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    dq2 = torch.empty_like(dq)
+    _lib.fa_bwd_two_pass(q, k, v, o, lse, dO, dq2, torch.empty_like(dk), torch.empty_like(dv), causal, scale, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq2), "two-pass dQ differs between two runs"
+    what = f"B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} {str(dtype)[6:]} causal={causal} two-pass"
+    _check_all(what, o, lse, (dq, dk, dv),
+               oracle.attention_fwd(x["q"], x["k"], x["v"], causal, scale),
+               oracle.attention_bwd(x["q"], x["k"], x["v"], x["dO"], causal, scale))
