@@ -200,20 +200,42 @@ def fp8_dequantized(q, k, v, signs):
     Hadamard (if ``signs`` is not None), each tensor quantised per tensor to
     e4m3 with sigma = amax / 448 and dequantised (fp64).
 
+    The e4m3 code of a value is an integer decided by floating point, so it
+    is decided in the precision the FP8 path uses, fp32 (the pages fix
+    none): with c = 1/sqrt(d) for a rotated tensor (1 otherwise) and x' the
+    value before that factor (the unnormalised transform, or the input),
+    amax = fl32(max |x'| * c), and the code is the nearest e4m3 value (ties
+    to even, saturating) of fl32(fl32(x' * c) * fl32(448 / amax)); sigma =
+    fl32(amax / 448).  Rounding x / sigma in fp64 instead splits exact ties
+    the other way: for 16-bit inputs without the rotation x * 448 / amax
+    often lies exactly on an e4m3 midpoint, which the fp64 quotient by the
+    rounded sigma misses by an ulp.
+
     Each tensor is handled one leading slice at a time, in two passes (the
     amax over all slices, then the rounding of each slice; the rotation and
     the rounding are per row), so the host memory needed is the fp64 output
     plus one slice."""
+    f32 = np.float32
 
     def qdq(x, rotate: bool):
-        def part(i):
-            return hadamard(x[i], signs) if rotate else _f64(x[i])
+        d = x.shape[-1]
+        c = f32(1.0 / np.sqrt(d)) if rotate else f32(1.0)
 
-        sigma = max(float(np.abs(part(i)).max()) for i in range(x.shape[0])) / 448.0
+        def part(i):  # x' in fp32
+            if rotate:
+                return (hadamard(x[i], signs) * np.sqrt(d)).astype(f32)
+            return _f64(x[i]).astype(f32)
+
+        amax = f32(max(f32(np.abs(part(i)).max()) for i in range(x.shape[0])) * c)
         out = np.empty(tuple(x.shape), dtype=np.float64)
+        if amax == 0.0:
+            out[...] = 0.0
+            return out
+        inv = f32(448.0) / amax
+        sigma = float(amax / f32(448.0))
         for i in range(x.shape[0]):
-            p = part(i)
-            out[i] = p if sigma == 0.0 else e4m3_round(p / sigma) * sigma
+            t = (part(i) * c) * inv  # two fp32 products, each rounded to nearest
+            out[i] = e4m3_round(t.astype(np.float64)) * sigma
         return out
 
     rot = signs is not None

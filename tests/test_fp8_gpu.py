@@ -3,7 +3,9 @@ oracle's dense Hadamard and e4m3 grid, and the FP8 forward against the fp64
 oracle.
 
 Tolerances: the quantised codes must be a correct rounding of the exact
-rotated value (within half an e4m3 ulp, plus fp32 noise).  The forward is
+rotated value (within half an e4m3 ulp, plus fp32 noise); without the
+rotation they must equal the oracle's codes exactly (both sides decide them
+in fp32, exact ties included).  The forward is
 gated on its relative RMS error ||O - O_model||_F / ||O_model||_F <= 0.03,
 where O_model is the exact fp64 attention of the inputs as the FP8 path holds
 them (the oracle's rotation and per-tensor e4m3 quantise-dequantise of Q, K
@@ -54,6 +56,13 @@ def test_hadamard_quant_matches_oracle(cuda_lib, d, rotate):
     tol = _e4m3_half_ulp(xr / sigma) * sigma * 1.001 + 1e-6 * sigma
     err = np.abs(deq - xr)
     assert (err <= tol).all(), f"{int((err > tol).sum())} codes off the nearest e4m3 value"
+    if not rotate:
+        # without the rotation every input is exact in fp32 and both sides
+        # decide the code in fp32 the same way: the codes (exact ties
+        # included) and the scale are identical
+        xm, _, _ = oracle.fp8_dequantized(x[None, None], x[None, None], x[None, None], None)
+        assert ds == float(np.float32(np.abs(x.double().numpy()).max()) / np.float32(448.0))
+        np.testing.assert_array_equal(deq, xm[0, 0])
 
 
 def _fp8_forward(x, signs, causal, scale):

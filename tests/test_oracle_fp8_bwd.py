@@ -256,7 +256,10 @@ def test_fp8_dequantized_matches_brute_force_per_tensor_scale():
     """The FP8 forward's input model: Q and K rotated (here by an explicit
     signed Sylvester matrix built in the test), then every tensor scaled by
     sigma = amax / 448, rounded to the nearest e4m3 value (brute force over the
-    grid) and scaled back; V is not rotated."""
+    grid) and scaled back; V is not rotated.  The rounding decision is taken
+    in fp32, as a product by the fp32 reciprocal 448 / amax after the 1/sqrt(d)
+    factor (numpy float32 arithmetic here)."""
+    f32 = np.float32
     rng = np.random.default_rng(17)
     d = 16
     q, k, v = (rng.standard_normal((1, 2, 24, d)) * s for s in (3.0, 0.2, 50.0))
@@ -264,9 +267,30 @@ def test_fp8_dequantized_matches_brute_force_per_tensor_scale():
     # range (|x / sigma| < 2^-6), so V gets a few of those
     v[0, 0, 0, :4] = np.abs(v).max() * np.array([1e-5, 2.5e-5, -3e-6, 1.7e-5])
     signs = np.where(rng.random(d) < 0.5, -1.0, 1.0)
-    H = np.array([[(-1.0) ** bin(i & j).count("1") for j in range(d)] for i in range(d)]) / np.sqrt(d)
+    Hs = np.array([[(-1.0) ** bin(i & j).count("1") for j in range(d)] for i in range(d)])
     qm, km, vm = oracle.fp8_dequantized(q, k, v, signs)
-    for got, x in ((qm, (q * signs) @ H), (km, (k * signs) @ H), (vm, v)):
-        sigma = np.abs(x).max() / 448.0
-        assert np.abs(x / sigma).max() == pytest.approx(448.0, rel=1e-15)
-        np.testing.assert_allclose(got, _nearest(x / sigma) * sigma, rtol=0, atol=1e-12 * np.abs(x).max())
+    for got, xp, c in ((qm, (q * signs) @ Hs, f32(1.0 / np.sqrt(d))), (km, (k * signs) @ Hs, f32(1.0 / np.sqrt(d))),
+                       (vm, v, f32(1.0))):
+        x32 = xp.astype(f32)
+        amax = f32(np.abs(x32).max() * c)
+        t = (x32 * c) * (f32(448.0) / amax)
+        assert np.abs(t).max() == pytest.approx(448.0, rel=1e-6)
+        want = _nearest(t.astype(np.float64)) * float(amax / f32(448.0))
+        np.testing.assert_array_equal(got, want)
+
+
+def test_fp8_dequantized_splits_exact_ties_to_even():
+    """16-bit values whose x * 448 / amax lies exactly on an e4m3 midpoint go
+    to the even code.  With amax = 122 (so sigma = 122 / 448 is not exact in
+    any binary format): 45.75 maps to exactly 168, halfway between 160 and
+    176, and 22.875 to exactly 84, halfway between 80 and 88; both go down to
+    the even codes 160 and 80.  47.6640625 maps to about 175.03 and goes to
+    the nearest value, 176; 30.5 maps to 112, on the grid."""
+    x = np.zeros((1, 1, 2, 8))
+    x[0, 0, 0, :5] = [122.0, 45.75, -45.75, 30.5, 22.875]
+    x[0, 0, 1, :2] = [47.6640625, 1.0]
+    xm, _, _ = oracle.fp8_dequantized(x, x, x, None)
+    sigma = float(np.float32(122.0) / np.float32(448.0))
+    codes = np.round(xm / sigma, 6)
+    np.testing.assert_array_equal(codes[0, 0, 0, :5], [448.0, 160.0, -160.0, 112.0, 80.0])
+    assert codes[0, 0, 1, 0] == 176.0
