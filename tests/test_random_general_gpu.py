@@ -1,8 +1,10 @@
 """Seeded random shapes for the general paths against the fp64 oracle: the
 causal sliding window (fa_fwd_local / fa_bwd_local), packed variable-length
 batches (fa_fwd_varlen / fa_bwd_varlen, with and without a window) and the
-deterministic two-pass backward (fa_bwd_two_pass) — and the FP8 path
-(Hadamard quantisation + fa_fwd_fp8) against the oracle's model of it.
+deterministic two-pass backward (fa_bwd_two_pass), the persistent forward at
+any length (fa_fwd_persistent), packed batches with a loose max_seqlen, the
+no-allocation backward (fa_bwd_noalloc) — and the FP8 path (Hadamard
+quantisation + fa_fwd_fp8) against the oracle's model of it.
 
 The draws cross the dispatch boundaries of these entry points: windows of 1
 key, short windows, windows on both sides of the persistent forward's 2048
@@ -188,3 +190,96 @@ def test_random_fp8_forward(cuda_lib, seed):
     dl = np.abs(lse.cpu().numpy() - lse_model)
     assert (dl <= 0.1).mean() >= 0.999, f"{what}: FP8 LSE off by more than 0.1 on {int((dl > 0.1).sum())} rows"
     assert (dl <= 0.1 + 1e-3 * np.abs(lse_model)).all(), f"{what}: FP8 LSE max diff {dl.max():.3f}"
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_persistent_forward(cuda_lib, seed):
+    """fa_fwd_persistent at any length (fa_fwd hands it only N <= 2048):
+    the oracle, and bit for bit fa_fwd, whose kernels do the same
+    arithmetic per block."""
+    g = np.random.default_rng(6000 + seed)
+    Hq, Hkv = _heads(g)
+    d, dtype = _elem(g)
+    N = int(g.choice([int(g.integers(1, 700)), int(g.integers(1900, 2200)), int(g.integers(2200, 4200))]))
+    B = 1 if N > 1500 else int(g.integers(1, 3))
+    causal = bool(g.integers(2))
+    x = make_custom(B, Hq, Hkv, N, d, dtype, seed=seed, with_grad=False)
+    q, k, v = (x[n].cuda().contiguous() for n in ("q", "k", "v"))
+    scale = d ** -0.5
+    outs = []
+    for fn in (_lib.fa_fwd_persistent, _lib.fa_fwd):
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+        fn(q, k, v, o, lse, causal, scale)
+        torch.cuda.synchronize()
+        assert _lib.fa_get_device_status() == _lib.FA_OK
+        outs.append((o, lse))
+    what = f"B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} {str(dtype)[6:]} causal={causal} persistent"
+    o_ref, lse_ref = oracle.attention_fwd(x["q"], x["k"], x["v"], causal, scale)
+    check_o(outs[0][0], o_ref, f"{what} O")
+    check_lse(outs[0][1], lse_ref, f"{what} LSE")
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1]), f"{what}: differs from fa_fwd"
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_packed_batch_loose_max_seqlen(cuda_lib, seed):
+    """max_seqlen is an upper bound on the lengths, not necessarily their
+    maximum: the same results as with the exact maximum."""
+    g = np.random.default_rng(7000 + seed)
+    Hq, Hkv = _heads(g)
+    d, dtype = _elem(g)
+    lengths = [int(g.choice([0, 1, int(g.integers(2, 700)), int(g.integers(700, 2100))]))
+               for _ in range(int(g.integers(1, 6)))]
+    if sum(lengths) == 0:
+        lengths[0] = 5
+    causal = bool(g.integers(2))
+    window = int(g.integers(1, 600)) if causal and g.integers(2) else 0
+    x = make_varlen(lengths, Hq, Hkv, d, dtype, seed=seed)
+    q, k, v, dO = (x[n].cuda().contiguous() for n in ("q", "k", "v", "dO"))
+    cu = x["cu_seqlens"].cuda()
+    total = q.shape[0]
+    scale = d ** -0.5
+    res = []
+    for max_len in (max(lengths), max(lengths) + int(g.integers(1, 3000))):
+        o = torch.empty_like(q)
+        lse = torch.empty((Hq, total), dtype=torch.float32, device="cuda")
+        _lib.fa_fwd_varlen(q, k, v, o, lse, cu, max_len, causal, scale, window)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(_lib.fa_bwd_varlen_workspace_bytes(total, Hq, d, True), dtype=torch.uint8, device="cuda")
+        _lib.fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu, max_len, causal, scale, True, ws, window)
+        torch.cuda.synchronize()
+        assert _lib.fa_get_device_status() == _lib.FA_OK
+        res.append((o, lse, dq, dk, dv))
+    what = f"lengths {lengths} Hq{Hq} Hkv{Hkv} d{d} causal={causal} W{window}"
+    _check_all(what, res[1][0], res[1][1], res[1][2:],
+               oracle.attention_fwd_varlen(x["q"], x["k"], x["v"], x["cu_seqlens"], causal, scale, window),
+               oracle.attention_bwd_varlen(x["q"], x["k"], x["v"], x["dO"], x["cu_seqlens"], causal, scale,
+                                           window))
+    # the deterministic backward and the forward do not depend on the bound
+    # (the kernels' tiles past a sequence's end are empty)
+    for a, b in zip(res[0], res[1]):
+        assert torch.equal(a, b), f"{what}: results depend on max_seqlen"
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_noalloc_backward(cuda_lib, seed):
+    g = np.random.default_rng(8000 + seed)
+    Hq, Hkv = _heads(g)
+    d, dtype = _elem(g)
+    N = int(g.choice([int(g.integers(1, 700)), int(g.integers(700, 1300)), int(g.integers(1900, 2600))]))
+    B = 1 if N > 1500 else int(g.integers(1, 3))
+    causal = bool(g.integers(2))
+    x = make_custom(B, Hq, Hkv, N, d, dtype, seed=seed)
+    q, k, v, dO = (x[n].cuda().contiguous() for n in ("q", "k", "v", "dO"))
+    scale = d ** -0.5
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+    _lib.fa_fwd(q, k, v, o, lse, causal, scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    _lib.fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, causal, scale)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    what = f"B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} {str(dtype)[6:]} causal={causal} no-alloc"
+    _check_all(what, o, lse, (dq, dk, dv),
+               oracle.attention_fwd(x["q"], x["k"], x["v"], causal, scale),
+               oracle.attention_bwd(x["q"], x["k"], x["v"], x["dO"], causal, scale))
