@@ -105,6 +105,31 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported element type {t.dtype}")
 
 
+def _need(name, t, dtypes=()):
+    """Refuses a tensor the C call cannot take: the library receives bare
+    pointers, so a wrong element type or a strided view would be read as
+    something else without any error."""
+    if t is None:
+        return
+    if dtypes and t.dtype not in dtypes:
+        raise TypeError(f"{name}: element type {t.dtype}, expected {' or '.join(str(x) for x in dtypes)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: tensor must be contiguous")
+
+
+def _io16(q, lse=None, f32=(), **same):
+    """Checks a 16-bit call's tensors (q's element type for `same`, fp32
+    for lse and `f32`) and returns q's type code."""
+    import torch
+    code = _dtype_code(q)
+    _need("q", q)
+    for name, t in same.items():
+        _need(name, t, (q.dtype,))
+    for name, t in (("lse", lse),) + tuple(f32):
+        _need(name, t, (torch.float32,))
+    return code
+
+
 def _dims(q, k):
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
@@ -114,15 +139,17 @@ def _dims(q, k):
 def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None):
     """O and LSE for q [B,Hq,N,d], k/v [B,Hkv,N,d] (contiguous CUDA tensors)."""
     B, Hq, Hkv, N, d = _dims(q, k)
+    code = _io16(q, lse, k=k, v=v, o=o)
     _check("fa_fwd", load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
-                                   int(causal), float(scale), _dtype_code(q), _stream(stream)))
+                                   int(causal), float(scale), code, _stream(stream)))
 
 
 def fa_fwd_persistent(q, k, v, o, lse, causal: bool, scale: float, stream=None):
     """fa_fwd as the persistent kernel (dynamic block schedule); same results."""
     B, Hq, Hkv, N, d = _dims(q, k)
+    code = _io16(q, lse, k=k, v=v, o=o)
     _check("fa_fwd_persistent", load().fa_fwd_persistent(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq,
-                                                         Hkv, N, d, int(causal), float(scale), _dtype_code(q),
+                                                         Hkv, N, d, int(causal), float(scale), code,
                                                          _stream(stream)))
 
 
@@ -130,24 +157,28 @@ def fa_fwd_f32_out(q, k, v, o_f32, lse, causal: bool, scale: float, stream=None)
     """fa_fwd with O written in fp32 (o_f32 [B,Hq,N,d] float32): the
     normalised accumulator before rounding to the input type."""
     B, Hq, Hkv, N, d = _dims(q, k)
+    code = _io16(q, lse, f32=(("o_f32", o_f32),), k=k, v=v)
     _check("fa_fwd_f32_out", load().fa_fwd_f32_out(_ptr(q), _ptr(k), _ptr(v), _ptr(o_f32), _ptr(lse), B, Hq, Hkv,
-                                                   N, d, int(causal), float(scale), _dtype_code(q), _stream(stream)))
+                                                   N, d, int(causal), float(scale), code, _stream(stream)))
 
 
 def fa_fwd_local(q, k, v, o, lse, window: int, scale: float, stream=None):
     """Causal sliding-window forward: row r sees keys r - window + 1 .. r."""
     B, Hq, Hkv, N, d = _dims(q, k)
+    code = _io16(q, lse, k=k, v=v, o=o)
     _check("fa_fwd_local", load().fa_fwd_local(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
-                                               int(window), float(scale), _dtype_code(q), _stream(stream)))
+                                               int(window), float(scale), code, _stream(stream)))
 
 
 def fa_bwd_local(q, k, v, o, lse, dO, dq, dk, dv, window: int, scale: float, deterministic: bool, workspace,
                  stream=None):
     B, Hq, Hkv, N, d = _dims(q, k)
+    code = _io16(q, lse, k=k, v=v, o=o, dO=dO, dq=dq, dk=dk, dv=dv)
+    _need("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("fa_bwd_local", load().fa_bwd_local(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d,
-        int(window), float(scale), _dtype_code(q), int(bool(deterministic)), _ptr(workspace), ws_bytes,
+        int(window), float(scale), code, int(bool(deterministic)), _ptr(workspace), ws_bytes,
         _stream(stream)))
 
 
@@ -155,12 +186,15 @@ def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens, max_seqlen: int, causal: bool, sc
                   stream=None):
     """Packed sequences: q/o [total,Hq,d], k/v [total,Hkv,d], lse [Hq,total],
     cu_seqlens int32 [B+1] on the device."""
+    import torch
     total, Hq, d = q.shape
     Hkv = k.shape[1]
     B = cu_seqlens.numel() - 1
+    code = _io16(q, lse, k=k, v=v, o=o)
+    _need("cu_seqlens", cu_seqlens, (torch.int32,))
     _check("fa_fwd_varlen", load().fa_fwd_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens), B, int(max_seqlen), total, Hq, Hkv, d,
-        int(causal), int(window), float(scale), _dtype_code(q), _stream(stream)))
+        int(causal), int(window), float(scale), code, _stream(stream)))
 
 
 def fa_bwd_varlen_workspace_bytes(total: int, Hq: int, d: int, deterministic: bool) -> int:
@@ -169,13 +203,17 @@ def fa_bwd_varlen_workspace_bytes(total: int, Hq: int, d: int, deterministic: bo
 
 def fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, cu_seqlens, max_seqlen: int, causal: bool, scale: float,
                   deterministic: bool, workspace, window: int = 0, stream=None):
+    import torch
     total, Hq, d = q.shape
     Hkv = k.shape[1]
     B = cu_seqlens.numel() - 1
+    code = _io16(q, lse, k=k, v=v, o=o, dO=dO, dq=dq, dk=dk, dv=dv)
+    _need("cu_seqlens", cu_seqlens, (torch.int32,))
+    _need("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("fa_bwd_varlen", load().fa_bwd_varlen(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens),
-        B, int(max_seqlen), total, Hq, Hkv, d, int(causal), int(window), float(scale), _dtype_code(q),
+        B, int(max_seqlen), total, Hq, Hkv, d, int(causal), int(window), float(scale), code,
         int(bool(deterministic)), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
@@ -185,10 +223,12 @@ def fa_bwd_workspace_bytes(B: int, Hq: int, N: int, d: int) -> int:
 
 def fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, workspace, stream=None):
     B, Hq, Hkv, N, d = _dims(q, k)
+    code = _io16(q, lse, k=k, v=v, o=o, dO=dO, dq=dq, dk=dk, dv=dv)
+    _need("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("fa_bwd", load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq),
                                    _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(causal), float(scale),
-                                   _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream)))
+                                   code, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def fa_bwd_two_pass_workspace_bytes(B: int, Hq: int, N: int, d: int) -> int:
@@ -198,10 +238,12 @@ def fa_bwd_two_pass_workspace_bytes(B: int, Hq: int, N: int, d: int) -> int:
 def fa_bwd_two_pass(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, workspace, stream=None):
     """Deterministic backward: dQ from a second pass over Q tiles, no atomics."""
     B, Hq, Hkv, N, d = _dims(q, k)
+    code = _io16(q, lse, k=k, v=v, o=o, dO=dO, dq=dq, dk=dk, dv=dv)
+    _need("workspace", workspace)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("fa_bwd_two_pass", load().fa_bwd_two_pass(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv,
-        N, d, int(causal), float(scale), _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream)))
+        N, d, int(causal), float(scale), code, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, stream=None):
@@ -209,16 +251,30 @@ def fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, causal: bool, scale: float, 
     caller workspace: for callers that cannot allocate device memory.  Calls
     that may overlap on the GPU race on that buffer."""
     B, Hq, Hkv, N, d = _dims(q, k)
+    code = _io16(q, lse, k=k, v=v, o=o, dO=dO, dq=dq, dk=dk, dv=dv)
     _check("fa_bwd_noalloc", load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
                                                    _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(causal),
-                                                   float(scale), _dtype_code(q), _stream(stream)))
+                                                   float(scale), code, _stream(stream)))
 
 
 def fa_hadamard_quant_workspace_bytes(rows: int, d: int) -> int:
     return int(load().fa_hadamard_quant_workspace_bytes(rows, d))
 
 
+def _byte_types():
+    import torch
+    return (torch.float8_e4m3fn, torch.uint8)
+
+
 def fa_hadamard_quant_fp8(x, signs, x8, descale, workspace, stream=None):
+    """x bf16 (the only input type of the C call), x8 e4m3 bytes, signs and
+    descale fp32."""
+    import torch
+    _need("x", x, (torch.bfloat16,))
+    _need("signs", signs, (torch.float32,))
+    _need("x8", x8, _byte_types())
+    _need("descale", descale, (torch.float32,))
+    _need("workspace", workspace)
     d = x.shape[-1]
     rows = x.numel() // d
     ws_bytes = workspace.numel() * workspace.element_size()
@@ -229,7 +285,13 @@ def fa_hadamard_quant_fp8(x, signs, x8, descale, workspace, stream=None):
 
 def fa_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, o, lse, causal: bool, scale: float,
                stream=None):
+    import torch
     B, Hq, Hkv, N, d = _dims(q8, k8)
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        _need(name, t, _byte_types())
+    for name, t in (("q_descale", q_descale), ("k_descale", k_descale), ("v_descale", v_descale), ("lse", lse)):
+        _need(name, t, (torch.float32,))
+    _need("o", o, (torch.bfloat16,))
     _check("fa_fwd_fp8", load().fa_fwd_fp8(
         _ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_descale), _ptr(k_descale), _ptr(v_descale), _ptr(o),
         _ptr(lse), B, Hq, Hkv, N, d, int(causal), float(scale), _stream(stream)))

@@ -311,7 +311,8 @@ def test_binding_marshals_shapes_dtypes_and_errors(monkeypatch):
     assert name == "fa_fwd" and a[0] == q.data_ptr() and a[4] == lse.data_ptr()
     assert a[5:] == (B, Hq, Hkv, N, d, 1, 0.25, _lib.FA_BF16, 7)
     ws = torch.zeros(300, dtype=torch.int32)
-    _lib.fa_bwd(q.half(), k, v, q, lse, q, q, k, v, False, 0.5, ws, stream=3)
+    qh, kh = q.half(), k.half()
+    _lib.fa_bwd(qh, kh, kh, qh, lse, qh, qh, kh, kh, False, 0.5, ws, stream=3)
     name, a = fake.calls[-1]
     assert a[9:] == (B, Hq, Hkv, N, d, 0, 0.5, _lib.FA_FP16, ws.data_ptr(), 1200, 3)
     total = 33
@@ -323,7 +324,7 @@ def test_binding_marshals_shapes_dtypes_and_errors(monkeypatch):
     assert a[9] == cu.data_ptr() and a[10:] == (2, 23, total, Hq, Hkv, d, 1, 5, pytest.approx(0.1), _lib.FA_BF16,
                                                 1, ws.data_ptr(), 1200, 1)
     x = torch.zeros(5, 7, 128, dtype=torch.bfloat16)
-    _lib.fa_hadamard_quant_fp8(x, None, x, lse, ws, stream=2)
+    _lib.fa_hadamard_quant_fp8(x, None, torch.zeros(5, 7, 128, dtype=torch.uint8), torch.zeros(1), ws, stream=2)
     name, a = fake.calls[-1]
     assert a[1] is None and a[4:] == (35, 128, ws.data_ptr(), 1200, 2)
     with pytest.raises(TypeError):
@@ -332,3 +333,40 @@ def test_binding_marshals_shapes_dtypes_and_errors(monkeypatch):
     with pytest.raises(_lib.FAError) as e:
         _lib.fa_fwd(q, k, v, q, lse, True, 0.25, stream=7)
     assert e.value.status == 2 and "FA_ERR_UNSUPPORTED" in str(e.value)
+
+
+def test_binding_refuses_wrong_element_types_and_strided_views():
+    """The C calls take bare pointers, so the binding checks what it hands
+    them: an fp16 tensor to the bf16-only quantiser, an output of another
+    type than the inputs, an LSE that is not fp32, or a strided view would
+    otherwise be read as something else with no error.  The checks run
+    before the library is called, so CPU tensors serve."""
+    import torch
+    from exact_attention_85_gb300 import _lib
+    x16 = torch.zeros(4, 128, dtype=torch.float16)
+    x8 = torch.zeros(4, 128, dtype=torch.uint8)
+    one = torch.zeros(1)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    with pytest.raises(TypeError, match="x: element type"):
+        _lib.fa_hadamard_quant_fp8(x16, None, x8, one, ws)
+    with pytest.raises(TypeError, match="x8: element type"):
+        _lib.fa_hadamard_quant_fp8(x16.to(torch.bfloat16), None, x8.float(), one, ws)
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 2, 8)
+    with pytest.raises(TypeError, match="o: element type"):
+        _lib.fa_fwd(q, q, q, q.half(), lse, True, 0.125)
+    with pytest.raises(TypeError, match="lse: element type"):
+        _lib.fa_fwd(q, q, q, q.clone(), lse.double(), True, 0.125)
+    with pytest.raises(TypeError, match="unsupported element type"):
+        _lib.fa_fwd(q.float(), q.float(), q.float(), q.float(), lse, True, 0.125)
+    strided = torch.zeros(1, 2, 64, 8, dtype=torch.bfloat16).transpose(2, 3)
+    with pytest.raises(ValueError, match="k: tensor must be contiguous"):
+        _lib.fa_fwd(q, strided, q, q.clone(), lse, True, 0.125)
+    with pytest.raises(TypeError, match="dq: element type"):
+        _lib.fa_bwd(q, q, q, q, lse, q, q.float(), q, q, True, 0.125, ws)
+    with pytest.raises(TypeError, match="cu_seqlens: element type"):
+        p = torch.zeros(8, 2, 64, dtype=torch.bfloat16)
+        _lib.fa_fwd_varlen(p, p, p, p.clone(), torch.zeros(2, 8), torch.tensor([0, 8]), 8, True, 0.125)
+    with pytest.raises(TypeError, match="o: element type"):
+        q8 = torch.zeros(1, 2, 8, 128, dtype=torch.uint8)
+        _lib.fa_fwd_fp8(q8, q8, q8, one, one, one, torch.zeros(1, 2, 8, 128), torch.zeros(1, 2, 8), False, 0.1)
