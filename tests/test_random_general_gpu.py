@@ -283,3 +283,34 @@ def test_random_noalloc_backward(cuda_lib, seed):
     _check_all(what, o, lse, (dq, dk, dv),
                oracle.attention_fwd(x["q"], x["k"], x["v"], causal, scale),
                oracle.attention_bwd(x["q"], x["k"], x["v"], x["dO"], causal, scale))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_random_large_query_groups(cuda_lib, seed):
+    """8 to 32 query heads per key/value head: the backward's CTAs walk the
+    Q tiles of every head of their group, and dK/dV sum over all of them."""
+    g = np.random.default_rng(13500 + seed)
+    d, dtype = _elem(g)
+    G = int(g.choice([8, 16, 32]))
+    Hkv = int(g.integers(1, 3))
+    Hq = G * Hkv
+    N = int(g.choice([int(g.integers(1, 400)), int(g.integers(400, 1300))]))
+    B = int(g.integers(1, 3))
+    causal = bool(g.integers(2))
+    deterministic = bool(g.integers(2))
+    x = make_custom(B, Hq, Hkv, N, d, dtype, seed=seed)
+    q, k, v, dO = (x[n].cuda().contiguous() for n in ("q", "k", "v", "dO"))
+    scale = d ** -0.5
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
+    _lib.fa_fwd(q, k, v, o, lse, causal, scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    size = (_lib.fa_bwd_two_pass_workspace_bytes if deterministic else _lib.fa_bwd_workspace_bytes)(B, Hq, N, d)
+    ws = torch.empty(size, dtype=torch.uint8, device="cuda")
+    (_lib.fa_bwd_two_pass if deterministic else _lib.fa_bwd)(q, k, v, o, lse, dO, dq, dk, dv, causal, scale, ws)
+    torch.cuda.synchronize()
+    assert _lib.fa_get_device_status() == _lib.FA_OK
+    what = f"B{B} Hq{Hq} Hkv{Hkv} N{N} d{d} {str(dtype)[6:]} causal={causal} deterministic={deterministic}"
+    _check_all(what, o, lse, (dq, dk, dv),
+               oracle.attention_fwd(x["q"], x["k"], x["v"], causal, scale),
+               oracle.attention_bwd(x["q"], x["k"], x["v"], x["dO"], causal, scale))
