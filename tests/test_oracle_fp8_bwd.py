@@ -261,7 +261,7 @@ def test_fp8_dequantized_matches_brute_force_per_tensor_scale():
     factor (numpy float32 arithmetic here)."""
     f32 = np.float32
     rng = np.random.default_rng(17)
-    d = 16
+    d = 32  # 1/sqrt(d) = 2^-2.5 is not a power of two, like the kernels' 2^-3.5 at d = 128
     q, k, v = (rng.standard_normal((1, 2, 24, d)) * s for s in (3.0, 0.2, 50.0))
     # a power-of-two change of sigma moves only values in e4m3's subnormal
     # range (|x / sigma| < 2^-6), so V gets a few of those
@@ -294,3 +294,40 @@ def test_fp8_dequantized_splits_exact_ties_to_even():
     codes = np.round(xm / sigma, 6)
     np.testing.assert_array_equal(codes[0, 0, 0, :5], [448.0, 160.0, -160.0, 112.0, 80.0])
     assert codes[0, 0, 1, 0] == 176.0
+
+
+# ------------------------------- planted mistakes in the forward's input model
+
+DQ_MUTANTS = {
+    "code_from_fp64_quotient": ("t = (part(i) * c) * inv  # two fp32 products",
+                                "t = part(i).astype(np.float64) * float(c) / (float(amax) / 448.0)  # "),
+    "value_without_inv_sqrt_d": ("t = (part(i) * c) * inv  # two fp32 products", "t = part(i) * inv  # "),
+    "amax_without_inv_sqrt_d": ("amax = f32(max(f32(np.abs(part(i)).max()) for i in range(x.shape[0])) * c)",
+                                "amax = f32(max(f32(np.abs(part(i)).max()) for i in range(x.shape[0])))"),
+    "sigma_off_grid_maximum": ("sigma = float(amax / f32(448.0))", "sigma = float(amax / f32(480.0))"),
+    "v_rotated": ("return qdq(q, rot), qdq(k, rot), qdq(v, False)", "return qdq(q, rot), qdq(k, rot), qdq(v, rot)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DQ_MUTANTS))
+def test_dequantized_pins_catch_planted_mistake(name, monkeypatch):
+    """Each mutant of the FP8 forward's input model (the fp32 code decision,
+    the 1/sqrt(d) factor, the scale, which tensors are rotated) fails the
+    brute-force pin or the exact-tie pin."""
+    import inspect
+    import types
+
+    old, new = DQ_MUTANTS[name]
+    src = inspect.getsource(oracle)
+    assert src.count(old) == 1, f"mutation anchor missing for {name}"
+    mod = types.ModuleType(f"oracle_mutant_{name}")
+    mod.__dict__["__file__"] = oracle.__file__
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
+    monkeypatch.setattr(oracle, "fp8_dequantized", mod.fp8_dequantized)
+    caught = 0
+    for pin in (test_fp8_dequantized_matches_brute_force_per_tensor_scale, test_fp8_dequantized_splits_exact_ties_to_even):
+        try:
+            pin()
+        except AssertionError:
+            caught += 1
+    assert caught > 0, f"no pin fails for {name}"
